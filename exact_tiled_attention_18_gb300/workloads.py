@@ -1,0 +1,106 @@
+"""Seeded synthetic inputs shaped like the FlashAttention pages' workloads.
+
+This module holds no attention arithmetic: it only draws random tensors and
+names the workload shapes.  Both the CUDA path and the fp64 checker consume
+the same bf16 tensors drawn here.
+
+Recipe: entries are i.i.d. N(0, 1), drawn in fp32 on the CPU with a seeded
+``torch.Generator`` and rounded once to bf16 (round to nearest even).  The
+long-context workload multiplies every 64th query row by 10 before the
+rounding, so that a row's running maximum jumps late in the sweep.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    backward: bool
+    boost_every: int = 0   # every k-th query row scaled (0 = none)
+    boost: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        """Softmax scale 1/sqrt(d), rounded to fp32 as the kernels receive it."""
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32))
+
+    def fwd_flops(self) -> float:
+        """Counted forward FLOPs: 4*B*H*N^2*d, halved when causal."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        """Counted backward FLOPs: 2.5x the forward count."""
+        return 2.5 * self.fwd_flops()
+
+
+# Shapes of the five workloads the method is measured on.
+WORKLOADS = {
+    "single_head_n256_d64": Workload("single_head_n256_d64", 1, 1, 256, 64, False, False),
+    "memory_exercise_n4096_d64": Workload("memory_exercise_n4096_d64", 1, 1, 4096, 64, False, False),
+    "memory_exercise_n4096_d64_causal": Workload("memory_exercise_n4096_d64_causal", 1, 1, 4096, 64, True, False),
+    "throughput_b8_h16_n4096_d64": Workload("throughput_b8_h16_n4096_d64", 8, 16, 4096, 64, False, False),
+    "throughput_b8_h16_n4096_d64_causal": Workload("throughput_b8_h16_n4096_d64_causal", 8, 16, 4096, 64, True, False),
+    "training_b4_h16_n8192_d128_causal": Workload("training_b4_h16_n8192_d128_causal", 4, 16, 8192, 128, True, True),
+    "long_context_b1_h32_n16384_d128_causal": Workload(
+        "long_context_b1_h32_n16384_d128_causal", 1, 32, 16384, 128, True, True, boost_every=64, boost=10.0),
+    "very_long_b1_h8_n65536_d128_causal": Workload("very_long_b1_h8_n65536_d128_causal", 1, 8, 65536, 128, True, False),
+}
+
+
+def randn_bf16(shape, seed: int) -> torch.Tensor:
+    """Seeded N(0,1) draw in fp32 on the CPU, rounded to bf16."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def make_inputs(B: int, H: int, N: int, d: int, seed: int = 0, with_grad: bool = False,
+                boost_every: int = 0, boost: float = 1.0) -> dict:
+    """Return CPU bf16 tensors q, k, v (and dO) of shape [B, H, N, d].
+
+    Each tensor has its own derived seed so that q, k, v and dO are
+    independent draws.  With ``boost_every`` = k > 0, query rows i with
+    i % k == 0 are multiplied by ``boost`` in fp32 before the bf16 rounding.
+    """
+    shape = (B, H, N, d)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    out = {}
+    names = ["q", "k", "v"] + (["do"] if with_grad else [])
+    for name in names:
+        x = torch.randn(*shape, generator=g, dtype=torch.float32)
+        if name == "q" and boost_every > 0:
+            x[:, :, ::boost_every, :] *= boost
+        out[name] = x.to(torch.bfloat16)
+    return out
+
+
+def workload_inputs(w: Workload, seed: int = 0) -> dict:
+    return make_inputs(w.B, w.H, w.N, w.d, seed=seed, with_grad=w.backward,
+                       boost_every=w.boost_every, boost=w.boost)
+
+
+def sample_rows(B: int, H: int, N: int, count: int, seed: int) -> list:
+    """Seeded sample of distinct (b, h, i) query rows, always including the
+    first and the last row of the first head."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) + 7919)
+    total = B * H * N
+    picks = {(0, 0, 0), (0, 0, N - 1)}
+    while len(picks) < min(count, total):
+        flat = int(torch.randint(0, total, (1,), generator=g))
+        bh, i = divmod(flat, N)
+        picks.add((bh // H, bh % H, i))
+    return sorted(picks)

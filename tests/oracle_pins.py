@@ -1,0 +1,284 @@
+"""Checks that pin the fp64 oracle to facts fixed outside itself.
+
+Each ``check_*`` takes an oracle module and raises AssertionError when the
+module disagrees with a fact the FlashAttention pages print, a closed form, an
+invariant of the mathematics, or a brute-force high-precision evaluation.
+``test_oracle.py`` runs them on the real oracle; ``test_oracle_mutants.py``
+runs them on copies of the oracle with a planted mistake and expects a
+failure, which shows that the pins would catch that kind of mistake.
+"""
+
+from __future__ import annotations
+
+import functools
+import json
+import math
+import os
+from fractions import Fraction
+
+import mpmath
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _bf16_values(shape, seed):
+    """Random values exactly representable in bf16 (and so in fp64/mpmath)."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(shape).astype(np.float32)
+    bits = x.view(np.uint32)
+    # round to nearest even on the top 16 bits
+    rounded = ((bits.astype(np.uint64) + 0x7FFF + ((bits >> 16) & 1)) >> 16) << 16
+    return rounded.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _head(x):
+    return x[None, None]
+
+
+# ---------------------------------------------------------------- worked example
+
+def check_two_tile_example(ora):
+    """Scores (0, ln 3) with values (2, 6) give 5; the same under causal
+    masking for the second query, and 2 for the first one."""
+    g = _golden("two_tile_example.json")
+    want = float(Fraction(g["output"]))
+    q = _head(np.array([[1.0], [1.0]]))
+    k = _head(np.array([[0.0], [math.log(3.0)]]))
+    v = _head(np.array([[float(g["tile1"]["value"])], [float(g["tile2"]["value"])]]))
+    o, lse = ora.forward(q, k, v, 1.0, False)
+    assert abs(o[0, 0, 0, 0] - want) < 1e-13, o
+    assert abs(o[0, 0, 1, 0] - want) < 1e-13, o
+    assert abs(lse[0, 0, 0] - math.log(4.0)) < 1e-13, lse
+    oc, lc = ora.forward(q, k, v, 1.0, True)
+    assert abs(oc[0, 0, 0, 0] - 2.0) < 1e-13, oc
+    assert abs(oc[0, 0, 1, 0] - want) < 1e-13, oc
+    assert abs(lc[0, 0, 0] - 0.0) < 1e-13, lc
+    # the full-softmax weights 1/4 and 3/4, recovered from the LSE
+    w = [math.exp(s - lse[0, 0, 0]) for s in (0.0, math.log(3.0))]
+    assert abs(w[0] - float(Fraction(g["full_softmax_weights"][0]))) < 1e-13
+    assert abs(w[1] - float(Fraction(g["full_softmax_weights"][1]))) < 1e-13
+
+
+def check_common_shift(ora):
+    """Adding 1000 to both scores leaves the output at 5."""
+    g = _golden("two_tile_example.json")
+    shift = float(g["common_shift"])
+    q = _head(np.array([[1.0], [1.0]]))
+    k = _head(np.array([[shift], [shift + math.log(3.0)]]))
+    v = _head(np.array([[2.0], [6.0]]))
+    o, lse = ora.forward(q, k, v, 1.0, False)
+    assert abs(o[0, 0, 0, 0] - float(Fraction(g["output_after_shift"]))) < 1e-12, o
+    assert abs(lse[0, 0, 0] - (shift + math.log(4.0))) < 1e-12, lse
+
+
+# ---------------------------------------------------------------- invariants
+
+def _random_case(b, h, n, d, seed):
+    shape = (b, h, n, d)
+    return (_bf16_values(shape, seed), _bf16_values(shape, seed + 1),
+            _bf16_values(shape, seed + 2), _bf16_values(shape, seed + 3))
+
+
+def check_rows_sum_to_one(ora):
+    """sum_j exp(s_ij - LSE_i) = 1 over eligible keys, with the scores formed
+    here by an explicit loop over the feature index."""
+    q, k, v, _ = _random_case(2, 2, 37, 8, 11)
+    scale = 0.3
+    for causal in (False, True):
+        _, lse = ora.forward(q, k, v, scale, causal)
+        s = np.zeros((2, 2, 37, 37))
+        for c in range(8):
+            s += q[..., :, None, c] * k[..., None, :, c]
+        s *= scale
+        if causal:
+            s = np.where(np.tril(np.ones((37, 37), dtype=bool)), s, -np.inf)
+        tot = np.exp(s - lse[..., None]).sum(-1)
+        assert np.max(np.abs(tot - 1.0)) < 1e-12, (causal, np.max(np.abs(tot - 1.0)))
+
+
+def check_equal_scores(ora):
+    """Q = 0 makes every score equal: O is the mean of the eligible V rows
+    (the prefix mean under causal masking) and LSE = ln(#eligible)."""
+    n, d = 29, 6
+    _, k, v, _ = _random_case(1, 2, n, d, 21)
+    q = np.zeros_like(k)
+    o, lse = ora.forward(q, k, v, 0.125, False)
+    assert np.max(np.abs(o - v.mean(axis=2, keepdims=True))) < 1e-13
+    assert np.max(np.abs(lse - math.log(n))) < 1e-13
+    oc, lc = ora.forward(q, k, v, 0.125, True)
+    counts = np.arange(1, n + 1, dtype=np.float64)
+    prefix_mean = np.cumsum(v, axis=2) / counts[None, None, :, None]
+    assert np.max(np.abs(oc - prefix_mean)) < 1e-13
+    assert np.max(np.abs(lc - np.log(counts)[None, None, :])) < 1e-13
+
+
+def check_causal_row0(ora):
+    """Under the causal mask query 0 sees only key 0: O_0 = V_0 and
+    LSE_0 = scale * <q_0, k_0>."""
+    q, k, v, _ = _random_case(1, 3, 17, 8, 31)
+    scale = 0.35355339059327373
+    o, lse = ora.forward(q, k, v, scale, True)
+    assert np.max(np.abs(o[:, :, 0] - v[:, :, 0])) < 1e-15
+    s00 = scale * np.array([[sum(q[0, h, 0, c] * k[0, h, 0, c] for c in range(8)) for h in range(3)]])
+    assert np.max(np.abs(lse[:, :, 0] - s00)) < 1e-14
+
+
+def check_causal_is_prefix(ora):
+    """Causal row i equals the non-causal answer on the first i+1 positions."""
+    q, k, v, _ = _random_case(1, 1, 12, 4, 41)
+    o, lse = ora.forward(q, k, v, 0.5, True)
+    for i in (0, 1, 5, 11):
+        oi, li = ora.forward(q[:, :, :i + 1], k[:, :, :i + 1], v[:, :, :i + 1], 0.5, False)
+        assert np.max(np.abs(o[:, :, i] - oi[:, :, i])) < 1e-13
+        assert abs(lse[0, 0, i] - li[0, 0, i]) < 1e-13
+
+
+def check_backward_row_identity(ora):
+    """sum_j P_ij dP_ij equals rowsum(dO * O) (the identity the preprocess
+    kernel uses), to fp64 rounding."""
+    q, k, v, do = _random_case(1, 2, 23, 8, 51)
+    for causal in (False, True):
+        o, _ = ora.forward(q, k, v, 0.4, causal)
+        _, _, _, dd = ora.backward(q, k, v, do, 0.4, causal)
+        assert np.max(np.abs(dd - (do * o).sum(-1))) < 1e-12
+
+
+def check_forward_rows_agree(ora):
+    """The sampled-row evaluation equals the full evaluation on those rows."""
+    q, k, v, _ = _random_case(2, 2, 19, 8, 61)
+    rows = [(0, 0, 0), (0, 1, 18), (1, 0, 7), (1, 1, 11)]
+    for causal in (False, True):
+        o, lse = ora.forward(q, k, v, 0.3, causal)
+        ro, rl = ora.forward_rows(q, k, v, 0.3, causal, rows)
+        for r, (b, h, i) in enumerate(rows):
+            assert np.max(np.abs(ro[r] - o[b, h, i])) < 1e-13
+            assert abs(rl[r] - lse[b, h, i]) < 1e-13
+
+
+# ---------------------------------------------------------------- brute force
+
+def _mp_forward(q, k, v, scale, causal):
+    """Definition evaluated entry by entry in 50-digit arithmetic (one head)."""
+    n, d, dv = len(q), len(q[0]), len(v[0])
+    o = [[None] * dv for _ in range(n)]
+    lse = [None] * n
+    for i in range(n):
+        keys = range(i + 1) if causal else range(n)
+        w = {}
+        for j in keys:
+            s = mpmath.mpf(0)
+            for c in range(d):
+                s += q[i][c] * k[j][c]
+            w[j] = mpmath.exp(scale * s)
+        tot = mpmath.fsum(w.values())
+        lse[i] = mpmath.log(tot)
+        for c in range(dv):
+            o[i][c] = mpmath.fsum(w[j] * v[j][c] for j in keys) / tot
+    return o, lse
+
+
+def _to_mp(a):
+    return [[mpmath.mpf(float(x)) for x in row] for row in a]
+
+
+@functools.lru_cache(maxsize=None)
+def _brute(n, d, causal, seed):
+    """50-digit forward values and central-difference gradients of
+    sum(O * dO) for one random head."""
+    mpmath.mp.dps = 50
+    q, k, v, do = (_bf16_values((n, d), seed + t) for t in range(4))
+    scale = mpmath.mpf(1) / mpmath.sqrt(d)
+    Q, K, V, DO = _to_mp(q), _to_mp(k), _to_mp(v), _to_mp(do)
+    o, lse = _mp_forward(Q, K, V, scale, causal)
+
+    def f(Q_, K_, V_):
+        oo, _ = _mp_forward(Q_, K_, V_, scale, causal)
+        return mpmath.fsum(oo[i][c] * DO[i][c] for i in range(n) for c in range(d))
+
+    h = mpmath.mpf("1e-18")
+    grads = []
+    for which in range(3):
+        g = np.zeros((n, d))
+        for i in range(n):
+            for c in range(d):
+                mats = [[row[:] for row in M] for M in (Q, K, V)]
+                x0 = mats[which][i][c]
+                mats[which][i][c] = x0 + h
+                fp = f(*mats)
+                mats[which][i][c] = x0 - h
+                fm = f(*mats)
+                g[i, c] = float((fp - fm) / (2 * h))
+        grads.append(g)
+    o_np = np.array([[float(x) for x in row] for row in o])
+    lse_np = np.array([float(x) for x in lse])
+    return (q, k, v, do, float(scale), o_np, lse_np) + tuple(grads)
+
+
+def _check_brute(ora, n, d, causal, seed):
+    q, k, v, do, scale, o_ref, lse_ref, dq_ref, dk_ref, dv_ref = _brute(n, d, causal, seed)
+    o, lse = ora.forward(_head(q), _head(k), _head(v), scale, causal)
+    assert np.max(np.abs(o[0, 0] - o_ref)) < 1e-13, np.max(np.abs(o[0, 0] - o_ref))
+    assert np.max(np.abs(lse[0, 0] - lse_ref)) < 1e-13
+    dq, dk, dv, _ = ora.backward(_head(q), _head(k), _head(v), _head(do), scale, causal)
+    for got, ref in ((dq, dq_ref), (dk, dk_ref), (dv, dv_ref)):
+        assert np.max(np.abs(got[0, 0] - ref)) < 1e-12, np.max(np.abs(got[0, 0] - ref))
+
+
+def check_brute_force_4x4(ora):
+    _check_brute(ora, 4, 4, False, 101)
+    _check_brute(ora, 4, 4, True, 201)
+
+
+def check_brute_force_8x8(ora):
+    _check_brute(ora, 8, 8, False, 301)
+    _check_brute(ora, 8, 8, True, 401)
+
+
+# ---------------------------------------------------------------- memory exercise
+
+def check_memory_exercise(ora):
+    g = _golden("memory_exercise.json")
+    n, d, b = g["N"], g["d"], g["bytes_per_element"]
+    mib = 1024 * 1024
+    assert ora.score_matrix_payload_bytes(n, b) == g["score_matrix_MiB"] * mib
+    assert ora.tensor_payload_bytes(n, d, b) == g["one_N_by_d_tensor_MiB"] * mib
+    assert 4 * ora.tensor_payload_bytes(n, d, b) == g["q_k_v_and_output_MiB"] * mib
+    assert ora.score_matrix_payload_bytes(n, b) // b == g["score_matrix_elements"]
+    assert ora.tensor_payload_bytes(n, d, b) // b == g["q_sized_tensor_elements"]
+    assert ora.score_matrix_payload_bytes(2 * n, b) == g["doubled_N_score_matrix_MiB"] * mib
+    assert ora.tensor_payload_bytes(2 * n, d, b) == g["doubled_N_q_sized_tensor_MiB"] * mib
+    assert ora.score_matrix_payload_bytes(8000, 1) == g["score_elements_8000_tokens"]
+    assert ora.score_matrix_payload_bytes(64000, 1) == g["score_elements_64000_tokens"]
+
+
+ALL_CHECKS = [
+    check_two_tile_example,
+    check_common_shift,
+    check_rows_sum_to_one,
+    check_equal_scores,
+    check_causal_row0,
+    check_causal_is_prefix,
+    check_backward_row_identity,
+    check_forward_rows_agree,
+    check_brute_force_4x4,
+    check_brute_force_8x8,
+    check_memory_exercise,
+]
+
+
+def failing_checks(ora):
+    """Names of the checks the given oracle module fails."""
+    bad = []
+    for chk in ALL_CHECKS:
+        try:
+            with np.errstate(all="ignore"):
+                chk(ora)
+        except Exception:  # AssertionError, or a crash caused by the mutation
+            bad.append(chk.__name__)
+    return bad
