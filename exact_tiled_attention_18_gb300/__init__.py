@@ -1,0 +1,15 @@
+"""Exact tiled attention for GB300 (sm_103a): C-ABI library + thin binding."""
+
+from .binding import (  # noqa: F401
+    FAError,
+    backward,
+    fa_bwd,
+    fa_bwd_workspace_bytes,
+    fa_fwd,
+    fa_last_failure,
+    fa_sched_enumerate,
+    fa_status_string,
+    fa_sync_status,
+    forward,
+    sync_status,
+)

@@ -1,0 +1,174 @@
+"""ctypes binding of libfa.so: the C ABI of include/fa.h, name for name.
+
+Argument marshalling only -- every step of the computation runs in the CUDA
+kernels behind these calls.  There is no fallback: if the library was not
+built (``python -m exact_tiled_attention_18_gb300.build``) every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED_D = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_LAUNCH = 4
+FA_ERR_TIMEOUT = 5
+FA_ERR_DEVICE_FAULT = 6
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    """A library call returned a status other than FA_OK."""
+
+    def __init__(self, call: str, status: int, text: str):
+        super().__init__(f"{call}: {text}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfa.so once; raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise FileNotFoundError(
+                f"{LIB_PATH} is missing: build it with `python -m exact_tiled_attention_18_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_fwd.restype = st
+        L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_bwd.restype = st
+        L.fa_bwd_workspace_bytes.argtypes = [i, i, i]
+        L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+        L.fa_sync_status.argtypes = [vp]
+        L.fa_sync_status.restype = st
+        L.fa_last_failure.argtypes = [ctypes.POINTER(ctypes.c_int)]
+        L.fa_last_failure.restype = st
+        L.fa_status_string.argtypes = [st]
+        L.fa_status_string.restype = ctypes.c_char_p
+        ll = ctypes.c_longlong
+        ip = ctypes.POINTER(ctypes.c_int)
+        L.fa_sched_enumerate.argtypes = [i, i, i, i, i, ll, ip, ip, ip, ll]
+        L.fa_sched_enumerate.restype = ll
+        _lib = L
+        return L
+
+
+def fa_status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def _check(call: str, status: int) -> None:
+    if status != FA_OK:
+        raise FAError(call, status, fa_status_string(status))
+
+
+def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: int, scale: float,
+           causal: int, stream: int) -> int:
+    """Raw C call; pointers and stream are integers.  Returns the status."""
+    return lib().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+
+
+def fa_bwd(q: int, k: int, v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int, workspace: int,
+           B: int, H: int, N: int, d: int, scale: float, causal: int, stream: int) -> int:
+    return lib().fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, N, d, scale, causal, stream)
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, H, N))
+
+
+def fa_sync_status(stream: int) -> int:
+    return lib().fa_sync_status(stream)
+
+
+def fa_last_failure() -> list:
+    out = (ctypes.c_int * 4)()
+    _check("fa_last_failure", lib().fa_last_failure(out))
+    return list(out)
+
+
+def fa_sched_enumerate(heads: int, N: int, d: int, causal: int, grid: int, l2_budget_bytes: int = 0):
+    """Host-only: list of (cta, head, pair) the kernels' scheduler deals."""
+    L = lib()
+    total = L.fa_sched_enumerate(heads, N, d, causal, grid, l2_budget_bytes, None, None, None, 0)
+    if total < 0:
+        raise ValueError("invalid scheduler arguments")
+    arr = [(ctypes.c_int * max(total, 1))() for _ in range(3)]
+    L.fa_sched_enumerate(heads, N, d, causal, grid, l2_budget_bytes, arr[0], arr[1], arr[2], total)
+    return [(arr[0][i], arr[1][i], arr[2][i]) for i in range(total)]
+
+
+# ----------------------------------------------------------------- torch side
+# PyTorch supplies device memory and the current stream; nothing else.
+
+def _stream_handle(device) -> int:
+    import torch
+    return int(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check_inputs(*ts):
+    import torch
+    ref = ts[0]
+    for t in ts:
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.shape != ref.shape \
+                or t.device != ref.device or t.dim() != 4:
+            raise ValueError("q, k, v (and dO) must be contiguous bf16 CUDA tensors of one shape [B, H, N, d]")
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None):
+    """O, LSE = attention(q, k, v) through fa_fwd on the current stream.
+
+    q, k, v: bf16 CUDA tensors [B, H, N, d].  Returns fp32 O [B, H, N, d]
+    and fp32 LSE [B, H, N].  ``out`` may supply preallocated (O, LSE).
+    """
+    import torch
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    if out is None:
+        o = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    _check("fa_fwd", fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            B, H, N, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, workspace=None,
+             out=None):
+    """dQ, dK, dV through fa_bwd on the current stream (fp32 outputs)."""
+    import torch
+    _check_inputs(q, k, v, do)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    if out is None:
+        dq, dk, dv = (torch.empty((B, H, N, d), dtype=torch.float32, device=q.device) for _ in range(3))
+    else:
+        dq, dk, dv = out
+    ws = workspace.data_ptr() if workspace is not None else 0
+    _check("fa_bwd", fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws,
+                            B, H, N, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    return dq, dk, dv
+
+
+def sync_status(device=None) -> None:
+    """Synchronise the current stream and raise if a kernel reported a failure."""
+    status = fa_sync_status(_stream_handle(device))
+    if status != FA_OK:
+        detail = fa_last_failure() if status == FA_ERR_TIMEOUT else None
+        raise FAError("fa_sync_status", status, fa_status_string(status) + (f" {detail}" if detail else ""))

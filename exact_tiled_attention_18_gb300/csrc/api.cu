@@ -1,0 +1,257 @@
+// C ABI of the library: argument checks, TMA descriptors, launches and the
+// device status word.  The operation each entry point computes is stated in
+// include/fa.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "internal.h"
+
+// Device status word written by the kernels when a bounded wait gives up:
+// [0] code, [1] wait site, [2] block, [3] work unit.  First failure wins.
+__device__ int g_fa_status[4];
+
+namespace {
+
+constexpr long long kDefaultL2Budget = 32LL << 20;  // K+V bytes of one L2 head group
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+int g_last_failure[4];
+
+fa_status device_info(DeviceInfo& out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FA_ERR_LAUNCH;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return FA_ERR_LAUNCH;
+    d.status = static_cast<int*>(p);
+    d.ready = true;
+  }
+  out = d;
+  return FA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 3-D view [heads][n][d] of a contiguous bf16 tensor; box = 64 columns x 128
+// rows x 1 head with 128-byte swizzle (the layout the MMA descriptors
+// expect).  Rows past n read as zeros.
+bool encode_bf16_map(CUtensorMap* m, const void* base, int heads, int n, int d) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(n) * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+unsigned long long wait_limit_ns() {
+  static unsigned long long v = []() -> unsigned long long {
+    const char* s = std::getenv("FA_WAIT_LIMIT_MS");
+    long long ms = s ? std::atoll(s) : 0;
+    if (ms <= 0) ms = 4000;
+    return static_cast<unsigned long long>(ms) * 1000000ULL;
+  }();
+  return v;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+fa_status check_sizes(int B, int H, int N, int d, int causal) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H * N >= (1LL << 31)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED_D;
+  return FA_OK;
+}
+
+fa::SchedParams make_sched(int heads, int n, int d, int causal, int grid_cap, long long budget) {
+  fa::SchedParams sp;
+  sp.heads = heads;
+  sp.units_per_head = (n + fa::kUnitRows - 1) / fa::kUnitRows;
+  sp.group_heads = fa::sched_group_heads(heads, n, d, budget > 0 ? budget : kDefaultL2Budget);
+  const long long units = static_cast<long long>(heads) * sp.units_per_head;
+  sp.grid = static_cast<int>(units < grid_cap ? units : grid_cap);
+  sp.causal = causal;
+  return sp;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, N, d, causal);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  DeviceInfo di;
+  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
+  const int heads = B * H;
+  fa::FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_bf16_map(&a.tm_q, q, heads, N, d) || !encode_bf16_map(&a.tm_k, k, heads, N, d) ||
+      !encode_bf16_map(&a.tm_v, v, heads, N, d))
+    return FA_ERR_LAUNCH;
+  a.o = o;
+  a.lse = lse;
+  a.n = N;
+  a.d = d;
+  a.causal = causal;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.sched = make_sched(heads, N, d, causal, di.sms, 0);
+  a.status = di.status;
+  a.wait_limit_ns = wait_limit_ns();
+  return fa::launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  if (static_cast<long long>(B) * H * N >= (1LL << 31)) return 0;
+  return static_cast<size_t>(B) * H * N * sizeof(float);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse, const void* dO,
+                 float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d, float scale,
+                 int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, N, d, causal);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) ||
+      (workspace && !aligned(workspace, 4)))
+    return FA_ERR_MISALIGNED;
+  DeviceInfo di;
+  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
+  const int heads = B * H;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  fa::BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_bf16_map(&a.tm_q, q, heads, N, d) || !encode_bf16_map(&a.tm_k, k, heads, N, d) ||
+      !encode_bf16_map(&a.tm_v, v, heads, N, d) || !encode_bf16_map(&a.tm_do, dO, heads, N, d))
+    return FA_ERR_LAUNCH;
+  float* delta = workspace;
+  if (!delta) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&delta), fa_bwd_workspace_bytes(B, H, N), s) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+  }
+  a.o = o;
+  a.lse = lse;
+  a.dout = static_cast<const uint16_t*>(dO);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.delta = delta;
+  a.heads = heads;
+  a.n = N;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.sched_kv = make_sched(heads, N, d, causal, di.sms, 0);
+  a.sched_q = a.sched_kv;
+  a.status = di.status;
+  a.wait_limit_ns = wait_limit_ns();
+  cudaError_t e = fa::launch_bwd(a, s);
+  if (!workspace) {
+    cudaError_t e2 = cudaFreeAsync(delta, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+fa_status fa_sync_status(fa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_DEVICE_FAULT;
+  int h[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(h, g_fa_status, sizeof(h)) != cudaSuccess) return FA_ERR_DEVICE_FAULT;
+  if (h[0] != 0) {
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      std::memcpy(g_last_failure, h, sizeof(h));
+    }
+    const int zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(g_fa_status, zero, sizeof(zero)) != cudaSuccess) return FA_ERR_DEVICE_FAULT;
+    return h[0] == FA_ERR_TIMEOUT ? FA_ERR_TIMEOUT : FA_ERR_DEVICE_FAULT;
+  }
+  return FA_OK;
+}
+
+fa_status fa_last_failure(int out[4]) {
+  if (!out) return FA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  std::memcpy(out, g_last_failure, sizeof(g_last_failure));
+  return FA_OK;
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK: success";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: null pointer or size/flag out of range";
+    case FA_ERR_UNSUPPORTED_D: return "FA_ERR_UNSUPPORTED_D: head dimension must be 64 or 128";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: tensor pointer breaks the 16-byte (4-byte) alignment rule";
+    case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: the CUDA runtime refused a launch or an allocation";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel pipeline wait ran past its limit";
+    case FA_ERR_DEVICE_FAULT: return "FA_ERR_DEVICE_FAULT: the stream reported a CUDA error";
+  }
+  return "unknown fa_status";
+}
+
+long long fa_sched_enumerate(int heads, int N, int d, int causal, int grid, long long l2_budget_bytes,
+                             int* out_cta, int* out_head, int* out_pair, long long capacity) {
+  if (heads < 1 || N < 1 || grid < 1 || (d != 64 && d != 128) || (causal != 0 && causal != 1)) return -1;
+  if (static_cast<long long>(heads) * N >= (1LL << 31)) return -1;
+  fa::SchedParams sp = make_sched(heads, N, d, causal, grid, l2_budget_bytes);
+  long long w = 0;
+  for (int c = 0; c < sp.grid; ++c) {
+    fa::SchedIter it = fa::sched_begin(sp);
+    int head, pair;
+    while (fa::sched_next(it, sp, c, head, pair)) {
+      if (w < capacity && out_cta && out_head && out_pair) {
+        out_cta[w] = c;
+        out_head[w] = head;
+        out_pair[w] = pair;
+      }
+      ++w;
+    }
+  }
+  return w;
+}
+
+}  // extern "C"

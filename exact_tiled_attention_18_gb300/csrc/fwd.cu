@@ -1,0 +1,441 @@
+// Forward kernel: exact attention, tile by tile, with an online softmax.
+//
+// Method (FlashAttention pages): Q, K and V are split into tiles that fit
+// on chip; each query tile sweeps the key/value tiles, keeping per row a
+// running maximum m, a running sum l of shifted exponentials and an
+// unnormalised accumulator, so the N x N score matrix never reaches HBM
+// ("FlashAttention Interview Questions: IO Complexity, Tiling, and Numerical
+// Stability", sections "How does tiling reduce IO?" and "How can softmax be
+// computed across tiles?"; "FlashAttention 1, 2 & 3", section 2 "Tiling &
+// Online Softmax" and "Kernel Fusion").  The update
+//   scale = exp(m - m_new); l = scale*l + sum exp(s - m_new);
+//   a = scale*a + sum exp(s - m_new) v;  output = a / l
+// is carried out in base 2 with a lazy reference: the reference maximum is
+// only moved (and l and the accumulator rescaled together) when a row's
+// maximum grows by more than 2^8, which keeps every exponent <= 8 and is
+// exact because numerator and denominator share the same reference.
+//
+// GB300 mapping.  One persistent CTA per SM.  A CTA takes two 128-row query
+// tiles (A and B) of one head at a time and streams the head's K/V tiles
+// through a ring of shared-memory slots filled by TMA.  Roles:
+//   warps 0-3  softmax for tile A   (thread = one query row = one TMEM lane)
+//   warps 4-7  softmax for tile B
+//   warp  8    TMA producer (one thread)
+//   warp  9    tcgen05 MMA issuer (one thread); owns the TMEM allocation
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [0,128) S_A, [128,256) S_B, [256,256+d) O_A, [256+d,256+2d) O_B.
+//   P (bf16, two per column) overwrites the first 64 columns of its S region
+//   and is the A operand of O += P V, read straight from TMEM.
+// While softmax A works on S_A(j), the tensor core runs PV_B(j-1) and
+// S_B(j); the two tiles ping-pong so MMA and exponentials overlap.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kFwdThreads = 320;
+constexpr float kTau = 8.0f;  // lazy-rescale threshold, log2 units
+constexpr float kLn2 = 0.69314718055994530942f;
+
+enum FwdSite : int {
+  SITE_LOAD_Q = 1,
+  SITE_LOAD_KV = 2,
+  SITE_MMA_Q = 3,
+  SITE_MMA_KV = 4,
+  SITE_MMA_P = 5,
+  SITE_SOFTMAX_S = 6,
+  SITE_SOFTMAX_O = 7,
+};
+
+template <int D>
+struct FwdLayout {
+  static constexpr int kTileBytes = kTileRows * D * 2;  // one bf16 tile of Q, K or V
+  static constexpr int kSlots = (D == 128) ? 4 : 8;     // K/V ring slots
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
+  // barrier indices
+  static constexpr int Q_FULL = 0;
+  static constexpr int Q_EMPTY = 1;
+  static constexpr int KV_FULL = 2;
+  static constexpr int KV_EMPTY = KV_FULL + kSlots;
+  static constexpr int S_FULL = KV_EMPTY + kSlots;
+  static constexpr int P_FULL = S_FULL + 2;
+  static constexpr int O_FULL = P_FULL + 2;
+  static constexpr int DRAIN = O_FULL + 2;
+  static constexpr int kNumBars = DRAIN + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+  static constexpr uint32_t kColO = 256;
+};
+
+__device__ __forceinline__ void unit_tiles(int pair, int nkt, bool causal, int& na, int& nb) {
+  if (causal) {
+    na = min(2 * pair + 1, nkt);
+    nb = min(2 * pair + 2, nkt);
+  } else {
+    na = nkt;
+    nb = nkt;
+  }
+}
+
+// Wait with every lane of the warp and agree on the outcome, so that the
+// warp-collective tcgen05 instructions after it are reached by all lanes or
+// by none.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w, int site, int unit) {
+  const bool ok = wait_bounded(bar, parity, w, site, unit);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait that ignores the abort flag: used only to let copies and MMAs
+// already in flight land before the CTA releases its resources.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, float* __restrict__ o, float* __restrict__ lse,
+               const int n, const float scale_log2, const SchedParams sp, int* status,
+               const unsigned long long limit_ns) {
+  using L = FwdLayout<D>;
+  constexpr int S = L::kSlots;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + L::kBarOff;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bars + 8 * L::Q_FULL, 1);
+    mbar_init(bars + 8 * L::Q_EMPTY, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bars + 8 * (L::KV_FULL + s), 1);
+      mbar_init(bars + 8 * (L::KV_EMPTY + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bars + 8 * (L::S_FULL + t), 1);
+      mbar_init(bars + 8 * (L::P_FULL + t), 128);
+      mbar_init(bars + 8 * (L::O_FULL + t), 1);
+    }
+    mbar_init(bars + 8 * L::DRAIN, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, status, limit_ns};
+  const int nkt = (n + kTileRows - 1) / kTileRows;
+  auto BAR = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+
+  if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    const int r = ((warp & 3) << 5) + lane;  // row inside the tile == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(t * 128);
+    const uint32_t tO = tmem + lane_off + L::kColO + static_cast<uint32_t>(t * D);
+    uint32_t sn = 0, on = 0;
+    SchedIter it = sched_begin(sp);
+    int head, pair;
+    bool ok = true;
+    while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
+      int na, nb;
+      unit_tiles(pair, nkt, CAUSAL, na, nb);
+      const int nt = t ? nb : na;
+      const int qtile = 2 * pair + t;
+      const int row = qtile * kTileRows + r;
+      const int unit = head * sp.units_per_head + pair;
+      float m_ref = 0.f, l = 0.f;
+      for (int j = 0; j < nt; ++j) {
+        ok = warp_wait(BAR(L::S_FULL + t), sn & 1, wc, SITE_SOFTMAX_S, unit);
+        if (!ok) break;
+        ++sn;
+        tc_fence_after();
+        uint32_t sr[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+        tmem_ld_wait();
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        const bool diag = CAUSAL && (j == qtile);
+        const bool tail = (j == nkt - 1) && ((n & (kTileRows - 1)) != 0);
+        if (diag || tail) {
+          const int lim = (CAUSAL ? min(row + 1, n) : n) - j * kTileRows;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -CUDART_INF_F;
+        }
+        float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, m2 = -CUDART_INF_F, m3 = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+          m0 = fmax3(m0, s[c + 0], s[c + 1]);
+          m1 = fmax3(m1, s[c + 2], s[c + 3]);
+          m2 = fmax3(m2, s[c + 4], s[c + 5]);
+          m3 = fmax3(m3, s[c + 6], s[c + 7]);
+        }
+        const float mt = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * scale_log2;
+        if (j == 0) {
+          m_ref = (mt == -CUDART_INF_F) ? 0.f : mt;
+        } else {
+          const bool need = mt > m_ref + kTau;
+          if (__any_sync(0xffffffffu, need)) {
+            // move the reference and rescale l and the accumulator together;
+            // PV of the previous tile is complete (its commit preceded S(j)'s)
+            const float m_new = fmaxf(m_ref, mt);
+            const float alpha = ex2_approx(m_ref - m_new);
+            m_ref = m_new;
+            l *= alpha;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tO + 32 * c, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+              tmem_st32(tO + 32 * c, v);
+            }
+            tmem_st_wait();
+          }
+        }
+        const float neg = -m_ref;
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            const float p0 = ex2_approx(fmaf(s[32 * c + 2 * i + 0], scale_log2, neg));
+            const float p1 = ex2_approx(fmaf(s[32 * c + 2 * i + 1], scale_log2, neg));
+            const float p2 = ex2_approx(fmaf(s[32 * c + 2 * i + 2], scale_log2, neg));
+            const float p3 = ex2_approx(fmaf(s[32 * c + 2 * i + 3], scale_log2, neg));
+            l0 += p0;
+            l1 += p1;
+            l2 += p2;
+            l3 += p3;
+            pk[i] = pack_bf16x2(p0, p1);
+            pk[i + 1] = pack_bf16x2(p2, p3);
+          }
+          tmem_st16(tS + 16 * c, pk);
+        }
+        l += (l0 + l1) + (l2 + l3);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR(L::P_FULL + t));
+      }
+      if (!ok) break;
+      // epilogue: O = accumulator / l, LSE = ln(sum exp(scaled scores))
+      ok = warp_wait(BAR(L::O_FULL + t), on & 1, wc, SITE_SOFTMAX_O, unit);
+      if (!ok) break;
+      ++on;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      const bool valid = row < n;
+      float* orow = o + (static_cast<size_t>(head) * n + row) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + 32 * c, v);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float4 w;
+            w.x = __uint_as_float(v[4 * i + 0]) * inv;
+            w.y = __uint_as_float(v[4 * i + 1]) * inv;
+            w.z = __uint_as_float(v[4 * i + 2]) * inv;
+            w.w = __uint_as_float(v[4 * i + 3]) * inv;
+            *reinterpret_cast<float4*>(orow + 32 * c + 4 * i) = w;
+          }
+        }
+      }
+      if (valid) lse[static_cast<size_t>(head) * n + row] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -CUDART_INF_F;
+    }
+  } else if (warp == 8) {
+    // -------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const uint64_t pol_q = l2_policy_evict_first();
+      uint32_t qn = 0, kvpos = 0;
+      SchedIter it = sched_begin(sp);
+      int head, pair;
+      bool ok = true;
+      while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
+        int na, nb;
+        unit_tiles(pair, nkt, CAUSAL, na, nb);
+        const int unit = head * sp.units_per_head + pair;
+        ok = wait_bounded(BAR(L::Q_EMPTY), (qn & 1) ^ 1, wc, SITE_LOAD_Q, unit);
+        if (!ok) break;
+        ++qn;
+        mbar_arrive_expect_tx(BAR(L::Q_FULL), 2 * L::kTileBytes);
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int kb = 0; kb < D / 64; ++kb)
+            tma_load_3d_hint(sbase + L::kQOff + t * L::kTileBytes + kb * 16384, &tm_q, BAR(L::Q_FULL), kb * 64,
+                             (2 * pair + t) * kTileRows, head, pol_q);
+        for (int j = 0; j < nb && ok; ++j) {
+#pragma unroll 1
+          for (int w = 0; w < 2; ++w) {
+            const uint32_t slot = kvpos % S, use = kvpos / S;
+            ok = wait_bounded(BAR(L::KV_EMPTY + slot), (use & 1) ^ 1, wc, SITE_LOAD_KV, unit);
+            if (!ok) break;
+            mbar_arrive_expect_tx(BAR(L::KV_FULL + slot), L::kTileBytes);
+            const CUtensorMap* tm = (w == 0) ? &tm_k : &tm_v;
+#pragma unroll
+            for (int kb = 0; kb < D / 64; ++kb)
+              tma_load_3d_hint(sbase + L::kRingOff + slot * L::kTileBytes + kb * 16384, tm,
+                               BAR(L::KV_FULL + slot), kb * 64, j * kTileRows, head, pol_kv);
+            ++kvpos;
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy already issued land before the CTA exits
+        if (qn > 0) drain_wait(BAR(L::Q_FULL), (qn - 1) & 1, limit_ns);
+        for (uint32_t s = 0; s < static_cast<uint32_t>(S); ++s) {
+          if (kvpos > s) {
+            const uint32_t last = kvpos - 1 - ((kvpos - 1 - s) % S);
+            drain_wait(BAR(L::KV_FULL + s), (last / S) & 1, limit_ns);
+          }
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
+      auto slot_addr = [&](uint32_t pos) -> uint32_t { return sbase + L::kRingOff + (pos % S) * L::kTileBytes; };
+      // S_t = Q_t K^T : M=128 query rows, N=128 keys, K=d (both K-major)
+      auto issue_s = [&](int t, uint32_t kaddr) {
+        const uint32_t qaddr = sbase + L::kQOff + t * L::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          umma_ss(tmem + static_cast<uint32_t>(t * 128), sdesc_sw128(qaddr + off, 16, 1024),
+                  sdesc_sw128(kaddr + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t V : M=128, N=d, K=128 keys; P from TMEM, V MN-major
+      auto issue_pv = [&](int t, uint32_t vaddr, bool acc) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          umma_ts(tmem + L::kColO + static_cast<uint32_t>(t * D), tmem + static_cast<uint32_t>(t * 128 + ks * 8),
+                  sdesc_sw128(vaddr + ks * 2048, kTileRows * 128, 1024), id_pv, (acc || ks > 0) ? 1u : 0u);
+        }
+      };
+      uint32_t qn = 0, kvbase = 0, pn0 = 0, pn1 = 0;
+      SchedIter it = sched_begin(sp);
+      int head, pair;
+      bool ok = true;
+      while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
+        int na, nb;
+        unit_tiles(pair, nkt, CAUSAL, na, nb);
+        const int unit = head * sp.units_per_head + pair;
+        ok = wait_bounded(BAR(L::Q_FULL), qn & 1, wc, SITE_MMA_Q, unit);
+        if (!ok) break;
+        ++qn;
+        ok = wait_bounded(BAR(L::KV_FULL + kvbase % S), (kvbase / S) & 1, wc, SITE_MMA_KV, unit);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(0, slot_addr(kvbase));
+        umma_commit(BAR(L::S_FULL + 0));
+        issue_s(1, slot_addr(kvbase));
+        umma_commit(BAR(L::S_FULL + 1));
+        for (int j = 0; j < nb; ++j) {
+          const uint32_t kpos = kvbase + 2 * j, vpos = kpos + 1, knext = kpos + 2;
+          const bool has_a = j < na, next_a = j + 1 < na, next_b = j + 1 < nb;
+          umma_commit(BAR(L::KV_EMPTY + kpos % S));  // K_j is free once S_B(j) completes
+          if (!next_b) umma_commit(BAR(L::Q_EMPTY));  // the unit's last S has been issued
+          ok = wait_bounded(BAR(L::KV_FULL + vpos % S), (vpos / S) & 1, wc, SITE_MMA_KV, unit);
+          if (!ok) break;
+          if (has_a) {
+            ok = wait_bounded(BAR(L::P_FULL + 0), pn0 & 1, wc, SITE_MMA_P, unit);
+            if (!ok) break;
+            ++pn0;
+            tc_fence_after();
+            issue_pv(0, slot_addr(vpos), j > 0);
+            if (!next_a) umma_commit(BAR(L::O_FULL + 0));
+            if (next_a) {
+              ok = wait_bounded(BAR(L::KV_FULL + knext % S), (knext / S) & 1, wc, SITE_MMA_KV, unit);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(0, slot_addr(knext));
+              umma_commit(BAR(L::S_FULL + 0));
+            }
+          }
+          ok = wait_bounded(BAR(L::P_FULL + 1), pn1 & 1, wc, SITE_MMA_P, unit);
+          if (!ok) break;
+          ++pn1;
+          tc_fence_after();
+          issue_pv(1, slot_addr(vpos), j > 0);
+          if (!next_b) umma_commit(BAR(L::O_FULL + 1));
+          umma_commit(BAR(L::KV_EMPTY + vpos % S));  // V_j is free once PV_B(j) completes
+          if (next_b) {
+            ok = wait_bounded(BAR(L::KV_FULL + knext % S), (knext / S) & 1, wc, SITE_MMA_KV, unit);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(1, slot_addr(knext));
+            umma_commit(BAR(L::S_FULL + 1));
+          }
+        }
+        kvbase += 2 * nb;
+      }
+      // every MMA this thread issued completes before tensor memory is freed
+      umma_commit(BAR(L::DRAIN));
+      drain_wait(BAR(L::DRAIN), 0, limit_ns);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  using L = FwdLayout<D>;
+  auto kern = fwd_kernel<D, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<a.sched.grid, kFwdThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.n,
+                                                             a.scale_log2, a.sched, a.status, a.wait_limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+  return a.causal ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+}
+
+}  // namespace fa

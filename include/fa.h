@@ -1,0 +1,137 @@
+/*
+ * fa.h -- C ABI of the exact tiled attention library for GB300 (sm_103a).
+ *
+ * The library computes, for every head of a [B, H, N, d] batch,
+ *
+ *     scores  = scale * Q K^T            (scale is normally 1/sqrt(d))
+ *     weights = row_softmax(scores + mask)
+ *     O       = weights V
+ *
+ * exactly (up to floating-point rounding order), tile by tile with an online
+ * softmax, so the N x N score matrix is never written to device memory.
+ * Source of the operation: "FlashAttention Interview Questions: IO
+ * Complexity, Tiling, and Numerical Stability", section "What is
+ * FlashAttention exact about?" (the three-line definition and the statement
+ * that the optimisation keeps the mathematical target, mask included), and
+ * "FlashAttention 1, 2 & 3: Memory Tiling & Eliminating the O(N^2) HBM
+ * Bottleneck", section 1 (Attention(Q,K,V) = softmax(QK^T/sqrt(d))V).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layout: every tensor is contiguous row-major [B][H][N][d]; the
+ *    log-sum-exp and the backward row term are [B][H][N].  One (b, h) pair
+ *    is one head; queries and keys have the same length N.
+ *  - Types: Q, K, V and dO are bf16 (raw 16-bit storage, `const void*`);
+ *    O, LSE, dQ, dK, dV and the workspace are fp32.
+ *  - Mask: causal = 0 means no mask; causal = 1 means query i sees key j iff
+ *    j <= i.  With this mask no row is ever fully masked.
+ *  - Sizes: B, H, N >= 1; d is 64 or 128; B*H*N < 2^31.
+ *  - Alignment: Q, K, V, dO, O, dQ, dK, dV must be 16-byte aligned; LSE and
+ *    the workspace 4-byte aligned.
+ *  - Ownership: every pointer is device memory owned by the caller.  The
+ *    library never frees caller memory and never allocates anything whose
+ *    size grows with N^2.
+ *  - Streams: work is queued on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and the calls return before it runs.
+ *  - Errors: argument errors are returned synchronously with nothing queued;
+ *    launch errors are returned synchronously.  A device-side failure (a
+ *    pipeline wait that ran past its time limit) is recorded in a status word
+ *    on the device and reported by fa_sync_status().  Every wait inside the
+ *    kernels is bounded (4 s by default; the FA_WAIT_LIMIT_MS environment
+ *    variable changes it), so a failing kernel returns instead of hanging.
+ *  - Thread safety: calls may be made from several host threads; calls on
+ *    different devices are independent.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,   /* null pointer, size out of range, causal not 0/1, scale not finite and > 0 */
+  FA_ERR_UNSUPPORTED_D = 2, /* d is not 64 or 128 */
+  FA_ERR_MISALIGNED = 3,    /* a pointer breaks the alignment rules above */
+  FA_ERR_LAUNCH = 4,        /* the CUDA runtime refused a launch or an allocation */
+  FA_ERR_TIMEOUT = 5,       /* a kernel wait ran past its limit; the kernel returned early */
+  FA_ERR_DEVICE_FAULT = 6   /* the stream reported a CUDA error while synchronising */
+} fa_status;
+
+/*
+ * Forward pass.
+ *   q, k, v : bf16 [B][H][N][d], read only.
+ *   o       : fp32 [B][H][N][d], written: O_i = sum_j softmax(s_i)_j v_j.
+ *   lse     : fp32 [B][H][N], written: LSE_i = ln sum_j exp(s_ij) over the
+ *             eligible keys (natural log of the scaled scores).  This is the
+ *             "compact normalization information" the backward pass keeps
+ *             ("FlashAttention Interview Questions ...", section "Why can
+ *             recomputation help training?").
+ *   scale   : multiplier of q.k, finite and > 0 (1/sqrt(d) in the pages'
+ *             definition).
+ * The online softmax follows the same page, section "How can softmax be
+ * computed across tiles?" (running maximum, rescaled sum and accumulator).
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H, int N, int d,
+                 float scale, int causal, fa_stream_t stream);
+
+/*
+ * Backward pass by recomputation: attention probabilities are rebuilt from
+ * q, k and the saved lse instead of being stored ("FlashAttention Interview
+ * Questions ...", section "Why can recomputation help training?").
+ *   q, k, v, dO : bf16 [B][H][N][d], read only (dO = dL/dO).
+ *   o, lse      : fp32 outputs of fa_fwd for the same q, k, v, scale, causal.
+ *   dq, dk, dv  : fp32 [B][H][N][d], overwritten with dL/dQ, dL/dK, dL/dV.
+ *   workspace   : fp32 buffer of fa_bwd_workspace_bytes(B, H, N) bytes that
+ *                 receives D_i = sum_c dO_ic O_ic; or NULL, in which case the
+ *                 library takes a stream-ordered allocation and frees it on
+ *                 the same stream.
+ * Computes P_ij = exp(s_ij - LSE_i), dV = P^T dO, dP = dO V^T,
+ * dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse, const void* dO,
+                 float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d, float scale,
+                 int causal, fa_stream_t stream);
+
+/* Bytes of the fa_bwd workspace: B*H*N fp32 values (0 on invalid sizes). */
+size_t fa_bwd_workspace_bytes(int B, int H, int N);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns FA_ERR_DEVICE_FAULT if the stream reported a CUDA
+ * error, FA_ERR_TIMEOUT if a kernel wait ran out since the last call, FA_OK
+ * otherwise.
+ */
+fa_status fa_sync_status(fa_stream_t stream);
+
+/*
+ * Details of the last device-side failure read by fa_sync_status():
+ * out[0] status code, out[1] wait site, out[2] block index, out[3] work unit.
+ * Returns FA_OK, or FA_ERR_INVALID_ARG if out is NULL.
+ */
+fa_status fa_last_failure(int out[4]);
+
+/* Static, human-readable name of a status code; never NULL. */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Host-only view of the persistent scheduler, for tests and tools (no GPU
+ * needed).  Deals the ceil(N/256) two-tile work units of each of `heads`
+ * heads to `grid` CTAs exactly as the forward kernel does.  Writes up to
+ * `capacity` triples (cta, head, pair) in dealing order and returns how many
+ * units exist in total, or -1 on invalid arguments.  l2_budget_bytes sets how
+ * many heads share an L2 group (0 = the library default).
+ */
+long long fa_sched_enumerate(int heads, int N, int d, int causal, int grid, long long l2_budget_bytes,
+                             int* out_cta, int* out_head, int* out_pair, long long capacity);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,137 @@
+"""Forward parity: CUDA path (through the C ABI) against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_tiled_attention_18_gb300 import workloads
+from tests.helpers import assert_forward_close, gpu_forward, scale_for, to64
+
+pytestmark = pytest.mark.gpu
+
+# (B, H, N, d, causal): several tiles, ragged tails, single rows, both d.
+SMALL = [
+    (1, 1, 256, 64, False),   # single-head workload
+    (1, 1, 256, 64, True),
+    (1, 1, 1, 64, False),
+    (1, 1, 1, 128, True),
+    (1, 1, 127, 128, True),
+    (1, 1, 128, 64, True),
+    (1, 1, 129, 128, False),
+    (2, 1, 129, 128, True),
+    (1, 2, 200, 64, True),
+    (1, 1, 255, 128, False),
+    (1, 1, 257, 64, True),
+    (1, 2, 300, 64, False),
+    (2, 2, 384, 128, False),
+    (1, 3, 517, 128, True),
+    (3, 1, 640, 64, False),
+    (1, 2, 1000, 128, True),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", SMALL)
+def test_forward_small_matches_oracle(B, H, N, d, causal):
+    inp = workloads.make_inputs(B, H, N, d, seed=N + 7 * d + causal)
+    scale = scale_for(d)
+    o, lse = gpu_forward(inp, causal, scale)
+    o_ref, lse_ref = oracle.forward(to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), scale, causal)
+    assert_forward_close(o.numpy(), lse.numpy(), o_ref, lse_ref, f"{(B, H, N, d, causal)}")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3, 4])
+def test_single_head_workload_seeds(seed):
+    w = workloads.WORKLOADS["single_head_n256_d64"]
+    inp = workloads.workload_inputs(w, seed)
+    o, lse = gpu_forward(inp, w.causal, w.scale)
+    o_ref, lse_ref = oracle.forward(to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), w.scale, w.causal)
+    assert_forward_close(o.numpy(), lse.numpy(), o_ref, lse_ref, f"seed {seed}")
+
+
+@pytest.mark.parametrize("name", ["memory_exercise_n4096_d64", "memory_exercise_n4096_d64_causal"])
+def test_memory_exercise_workload(name):
+    w = workloads.WORKLOADS[name]
+    inp = workloads.workload_inputs(w, 0)
+    o, lse = gpu_forward(inp, w.causal, w.scale)
+    o_ref, lse_ref = oracle.forward(to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), w.scale, w.causal)
+    assert_forward_close(o.numpy(), lse.numpy(), o_ref, lse_ref, name)
+
+
+def _sampled(w, seed, count):
+    inp = workloads.workload_inputs(w, seed)
+    o, lse = gpu_forward(inp, w.causal, w.scale)
+    rows = workloads.sample_rows(w.B, w.H, w.N, count, seed)
+    ro, rl = oracle.forward_rows(to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), w.scale, w.causal, rows)
+    idx = tuple(np.array(rows).T)
+    assert_forward_close(o.numpy()[idx], lse.numpy()[idx], ro, rl, w.name)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("name", [
+    "throughput_b8_h16_n4096_d64",
+    "throughput_b8_h16_n4096_d64_causal",
+    "training_b4_h16_n8192_d128_causal",
+    "long_context_b1_h32_n16384_d128_causal",
+    "very_long_b1_h8_n65536_d128_causal",
+])
+def test_full_size_sampled_rows(name):
+    _sampled(workloads.WORKLOADS[name], 0, 256)
+
+
+def test_late_large_maximum_rescales():
+    """A key in the last tile whose score dwarfs every earlier one moves the
+    running maximum late in the sweep (rescaling path)."""
+    inp = workloads.make_inputs(1, 2, 700, 128, seed=11)
+    inp["k"][:, :, 690, :] = (inp["q"][:, :, 699, :].float() * 3).to(torch.bfloat16)
+    scale = scale_for(128)
+    for causal in (False, True):
+        o, lse = gpu_forward(inp, causal, scale)
+        o_ref, lse_ref = oracle.forward(to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), scale, causal)
+        assert_forward_close(o.numpy(), lse.numpy(), o_ref, lse_ref, f"late max causal={causal}")
+
+
+def test_masked_positions_do_not_leak():
+    """Extreme values at causally masked K/V positions leave eligible outputs unchanged."""
+    B, H, N, d = 1, 1, 300, 64
+    inp = workloads.make_inputs(B, H, N, d, seed=3)
+    scale = scale_for(d)
+    o1, l1 = gpu_forward(inp, True, scale)
+    poisoned = {k: v.clone() for k, v in inp.items()}
+    # keys >= 160 are invisible to queries < 160 (160 is also a warp boundary,
+    # so no warp-wide rescale decision can couple the two groups of rows)
+    poisoned["k"][:, :, 160:, :] = 1e4
+    poisoned["v"][:, :, 160:, :] = -1e4
+    o2, l2 = gpu_forward(poisoned, True, scale)
+    assert torch.equal(o1[:, :, :160], o2[:, :, :160])
+    assert torch.equal(l1[:, :, :160], l2[:, :, :160])
+
+
+def test_head_result_independent_of_batch_position():
+    """A head computed alone equals the same head inside a larger batch
+    (different CTA and scheduling)."""
+    inp = workloads.make_inputs(2, 3, 384, 128, seed=5)
+    scale = scale_for(128)
+    o, lse = gpu_forward(inp, True, scale)
+    one = {k: v[1:2, 2:3].contiguous() for k, v in inp.items()}
+    o1, l1 = gpu_forward(one, True, scale)
+    assert torch.equal(o[1:2, 2:3], o1) and torch.equal(lse[1:2, 2:3], l1)
+
+
+def test_forward_allocates_nothing():
+    """The forward call allocates no device memory: no N x N buffer, no workspace."""
+    w = workloads.WORKLOADS["memory_exercise_n4096_d64"]
+    inp = workloads.workload_inputs(w, 0)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    import exact_tiled_attention_18_gb300 as fa
+    o = torch.empty((1, 1, 4096, 64), dtype=torch.float32, device="cuda")
+    lse = torch.empty((1, 1, 4096), dtype=torch.float32, device="cuda")
+    fa.forward(q, k, v, out=(o, lse))
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        fa.forward(q, k, v, out=(o, lse))
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free0 - free1 < 1 << 20
+    fa.sync_status()
