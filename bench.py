@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Attention TFLOP/s on GB300: forward + backward of exact tiled attention.
+
+One step is one pass of the whole path over one batch: fa_fwd (O, LSE) then
+fa_bwd (D preprocess, dK/dV, dQ).  Counted FLOPs: 4*B*H*N^2*d for the
+forward, halved when causal, and 2.5x that for the backward.  Default
+workload: B=4, H=16, N=8192, d=128, causal, bf16 inputs ~ N(0,1).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--fwd-only]
+
+Prints one JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
+oracle (the only reference implementation there is) on a bounded sample of
+the same workload.  Under torchrun each rank runs its own batch (heads are
+independent: no collective on the data path) and the line reports the
+aggregate over ranks with the time of the slowest rank.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 and fraction of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "training_b4_h16_n8192_d128_causal"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--fwd-only", action="store_true", help="time the forward pass alone")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("bf16_tflops", "bf16_tflops_sustained", "hbm_gbs")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_tiled_attention_18_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_tag):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is missing or was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None
+    m_src = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_src or not m_b or m_src.group(1) != kernel_source_digest():
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        # samples taken while the GPU is busy: the upper half of the clock trace
+        busy = sorted(sm)[len(sm) // 2:] if len(sm) > 4 else sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(rank, world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29531")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(value, dist, device=None):
+    """Largest value across ranks (the slowest rank's time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w, seed, budget_s):
+    """Time the fp64 oracle on whole heads of the workload, one head at a
+    time, until about `budget_s` seconds of CPU work; returns (TFLOP/s of
+    counted FLOPs, heads, seconds, what)."""
+    import numpy as np
+    import oracle
+    from exact_tiled_attention_18_gb300 import workloads
+    inp = workloads.make_inputs(1, 1, w.N, w.d, seed=seed, with_grad=True,
+                                boost_every=w.boost_every, boost=w.boost)
+    x = {n: inp[n].float().double().numpy() for n in inp}
+    heads, t_total = 0, 0.0
+    while heads < 4 and (heads == 0 or t_total < budget_s):
+        t0 = time.perf_counter()
+        o, lse = oracle.forward(x["q"], x["k"], x["v"], w.scale, w.causal)
+        if w.backward:
+            oracle.backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal)
+        t_total += time.perf_counter() - t0
+        heads += 1
+    flops_head = w.fwd_flops() / (w.B * w.H) + (w.bwd_flops() / (w.B * w.H) if w.backward else 0.0)
+    np.asarray(o)
+    return flops_head * heads / t_total / 1e12, heads, t_total
+
+
+def oracle_threads():
+    n = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    try:
+        from threadpoolctl import threadpool_info
+        blas = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if blas:
+            return int(blas[0])
+    except Exception:
+        pass
+    return int(n)
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import exact_tiled_attention_18_gb300 as fa
+    from exact_tiled_attention_18_gb300 import workloads
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(rank, world, "nccl")
+    w = workloads.WORKLOADS[args.workload]
+    do_bwd = w.backward and not args.fwd_only
+    peaks, peak_kind = load_peaks()
+
+    # inputs resident in HBM before the timed region (each rank its own batch)
+    inp = workloads.workload_inputs(w, seed=rank)
+    q, k, v = (inp[n].to(device) for n in ("q", "k", "v"))
+    dout = inp["do"].to(device) if do_bwd else None
+    B, H, N, d = w.B, w.H, w.N, w.d
+    o = torch.empty((B, H, N, d), dtype=torch.float32, device=device)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=device)
+    if do_bwd:
+        dq, dk, dv = (torch.empty((B, H, N, d), dtype=torch.float32, device=device) for _ in range(3))
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N) // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    launches_per_step = 1 + (3 if do_bwd else 0)
+
+    ev = []
+
+    def step(record):
+        if record:
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+        fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=(o, lse))
+        if record:
+            e1.record(stream)
+        if do_bwd:
+            fa.backward(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale, workspace=ws, out=(dq, dk, dv))
+        if record:
+            e2.record(stream)
+            ev.append((e0, e1, e2))
+
+    for _ in range(args.warmup):
+        step(False)
+    fa.sync_status(device)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.start()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop() if sampler else None
+    barrier(dist, device)
+    fa.sync_status(device)
+
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, device)
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
+    bwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev) if do_bwd else 0.0
+    ms_per_step = total_ms / args.steps
+    step_flops = w.fwd_flops() + (w.bwd_flops() if do_bwd else 0.0)
+    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, results out
+    e2e = None
+    if args.e2e_steps > 0:
+        names = ["q", "k", "v"] + (["do"] if do_bwd else [])
+        host_in = {n: inp[n].pin_memory() for n in names}
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    for t in ([o, lse] + ([dq, dk, dv] if do_bwd else []))]
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            qq, kk, vv = (host_in[n].to(device, non_blocking=True) for n in ("q", "k", "v"))
+            oo, ll = fa.forward(qq, kk, vv, causal=w.causal, scale=w.scale)
+            outs = [oo, ll]
+            if do_bwd:
+                dd = host_in["do"].to(device, non_blocking=True)
+                outs += list(fa.backward(qq, kk, vv, oo, ll, dd, causal=w.causal, scale=w.scale))
+            for h, g in zip(host_out, outs):
+                h.copy_(g, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        fa.sync_status(device)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), dist, device) / args.e2e_steps
+        e2e = {"value": round(step_flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, heads, secs = oracle_sample(w, 0, 10.0)
+        cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"{heads} whole head(s) of the workload (N={w.N}, d={w.d}, causal={w.causal}), "
+                         f"{'forward+backward' if do_bwd else 'forward'} in numpy fp64, {secs:.1f} s"}
+
+    if rank != 0:
+        return None
+    sustained = peaks["bf16_tflops_sustained"]
+    burst = peaks["bf16_tflops"]
+    fwd_tflops = w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
+    bwd_tflops = w.bwd_flops() / (bwd_ms * 1e-3) / 1e12 if do_bwd else None
+    # dominant kernel: the one with the larger share of the step
+    if do_bwd and bwd_ms > fwd_ms:
+        dom = {"kernel": "fa_bwd (preprocess + dK/dV + dQ)", "ms": bwd_ms, "tflops": bwd_tflops,
+               "tag": f"bwd_kernels_{w.name}"}
+    else:
+        dom = {"kernel": "fwd_kernel", "ms": fwd_ms, "tflops": fwd_tflops, "tag": f"fwd_kernel_{w.name}"}
+    roofline = {"bound": "tensor", "kernel": dom["kernel"], "achieved": round(dom["tflops"], 2),
+                "peak": sustained, "unit": "TFLOP/s", "frac": round(dom["tflops"] / sustained, 4),
+                "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long loop)",
+                "frac_of_burst_peak": round(dom["tflops"] / burst, 4),
+                "traffic": ncu_traffic(dom["tag"])}
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "step": "fwd+bwd" if do_bwd else "fwd",
+                   "l2": f"inputs {3 * w.B * w.H * w.N * w.d * 2 / 2**20:.0f} MiB of Q,K,V > L2; no flush",
+                   "parallelism": f"heads independent; {world} rank(s) x own batch, no collective"},
+        "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fwd_tflops, 2),
+                "frac_of_sustained": round(fwd_tflops / sustained, 4), "frac_of_burst": round(fwd_tflops / burst, 4)},
+        "bwd": ({"ms": round(bwd_ms, 4), "tflops": round(bwd_tflops, 2),
+                 "frac_of_sustained": round(bwd_tflops / sustained, 4)} if do_bwd else None),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    return line
+
+
+# ----------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return None
+    from exact_tiled_attention_18_gb300 import workloads
+    import oracle
+    w = workloads.WORKLOADS[args.workload]
+    do_bwd = w.backward and not args.fwd_only
+    # each step: the fp64 oracle on a causal prefix of one head (the first
+    # `prefix` positions), a bounded sample of the workload
+    prefix = min(w.N, 2048)
+    inp = workloads.make_inputs(1, 1, prefix, w.d, seed=0, with_grad=True,
+                                boost_every=w.boost_every, boost=w.boost)
+    x = {n: inp[n].float().double().numpy() for n in inp}
+    mult = 1.0 if w.causal else 2.0
+    flops = 2.0 * mult * prefix * prefix * w.d * (1.0 + (2.5 if do_bwd else 0.0))
+
+    def step():
+        oracle.forward(x["q"], x["k"], x["v"], w.scale, w.causal)
+        if do_bwd:
+            oracle.backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = time.perf_counter() - t0
+    ms = secs * 1e3 / args.steps
+    value = flops / (ms * 1e-3) / 1e12
+    sample = (f"fp64 numpy oracle on the first {prefix} positions of one head (N={w.N}, d={w.d}, "
+              f"causal={w.causal}), {'forward+backward' if do_bwd else 'forward'} per step")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "step": "fwd+bwd" if do_bwd else "fwd"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

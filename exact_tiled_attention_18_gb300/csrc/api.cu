@@ -98,10 +98,12 @@ fa_status check_sizes(int B, int H, int N, int d, int causal) {
   return FA_OK;
 }
 
-fa::SchedParams make_sched(int heads, int n, int d, int causal, int grid_cap, long long budget) {
+fa::SchedParams make_sched(int heads, int n, int d, int causal, int grid_cap, long long budget,
+                           int unit_rows = fa::kUnitRows, int cost_grows = 1) {
   fa::SchedParams sp;
   sp.heads = heads;
-  sp.units_per_head = (n + fa::kUnitRows - 1) / fa::kUnitRows;
+  sp.units_per_head = (n + unit_rows - 1) / unit_rows;
+  sp.cost_grows = cost_grows;
   sp.group_heads = fa::sched_group_heads(heads, n, d, budget > 0 ? budget : kDefaultL2Budget);
   const long long units = static_cast<long long>(heads) * sp.units_per_head;
   sp.grid = static_cast<int>(units < grid_cap ? units : grid_cap);
@@ -185,8 +187,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const float* o, co
   a.causal = causal;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.sched_kv = make_sched(heads, N, d, causal, di.sms, 0);
-  a.sched_q = a.sched_kv;
+  // dK/dV: one unit per 128-key tile, heaviest at the start of the sequence;
+  // dQ: one unit per 128-query tile, heaviest at the end.
+  a.sched_kv = make_sched(heads, N, d, causal, di.sms, 0, fa::kTileRows, 0);
+  a.sched_q = make_sched(heads, N, d, causal, di.sms, 0, fa::kTileRows, 1);
+  a.grid_kv = a.sched_kv.grid;
+  a.grid_q = a.sched_q.grid;
+  a.grid_pre = 2 * di.sms;
   a.status = di.status;
   a.wait_limit_ns = wait_limit_ns();
   cudaError_t e = fa::launch_bwd(a, s);

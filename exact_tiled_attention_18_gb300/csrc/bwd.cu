@@ -1,10 +1,834 @@
-// Backward kernels (placeholder until the tcgen05 backward lands).
+// Backward pass by recomputation.
+//
+// The forward pass keeps only O and the per-row log-sum-exp; the backward
+// pass rebuilds the attention probabilities from Q, K and that LSE instead
+// of storing the N x N matrices ("FlashAttention Interview Questions: IO
+// Complexity, Tiling, and Numerical Stability", section "Why can
+// recomputation help training?").  With P_ij = exp(s_ij - LSE_i):
+//   dV = P^T dO,  dP = dO V^T,  D_i = sum_c dO_ic O_ic,
+//   dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+// (D_i = sum_j P_ij dP_ij equals rowsum(dO o O) because O = P V.)
+//
+// Three kernels, in stream order:
+//   preprocess  D' = rowsum(dO o O)                        (HBM bound)
+//   dkdv        one CTA per 128-key tile, sweeping the query tiles that
+//               see it: S^T = K Q^T and dP^T = V dO^T on tcgen05 into TMEM,
+//               P^T and dS^T computed by two warpgroups (thread = key row)
+//               and written back to TMEM as bf16 (dS^T as a hi + lo pair),
+//               then dV += P^T dO and dK += (dS^T hi + dS^T lo) Q with the A
+//               operand read from TMEM.
+//   dq          one CTA per 128-query tile, sweeping its key tiles:
+//               S = Q K^T, dP = dO V^T, dS (hi + lo) in TMEM, dQ += dS K;
+//               it also corrects D' to the exact row term (see the kernel)
+//               and so runs before dkdv.
+// Every pipeline wait is bounded, as in the forward kernel.
 #include <cuda_runtime.h>
+#include <math_constants.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace fa {
+namespace {
 
-cudaError_t launch_bwd(const BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum BwdSite : int {
+  SITE_KV_LOAD_KV = 11,
+  SITE_KV_LOAD_QD = 12,
+  SITE_KV_LD_EMPTY = 13,
+  SITE_KV_MMA_KV = 14,
+  SITE_KV_MMA_QD = 15,
+  SITE_KV_MMA_PDS = 16,
+  SITE_KV_EW_LD = 17,
+  SITE_KV_EW_SDP = 18,
+  SITE_KV_EW_ACC = 19,
+  SITE_Q_LOAD_Q = 21,
+  SITE_Q_LOAD_KV = 22,
+  SITE_Q_MMA_Q = 23,
+  SITE_Q_MMA_KV = 24,
+  SITE_Q_MMA_DS = 25,
+  SITE_Q_EW_SDP = 26,
+  SITE_Q_EW_ACC = 27,
+  SITE_Q_EW_XCH = 28,
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w, int site, int unit) {
+  const bool ok = wait_bounded(bar, parity, w, site, unit);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
+
+// Two-term bf16 split of a pair of fp32 values: hi keeps the top 16 bits of
+// each value (truncation), lo is the exact remainder rounded to bf16, so
+// hi + lo carries about 16 significant bits.  dS feeds the dK and dQ
+// products this way: rows with large |q| (the long-context workload scales
+// every 64th query by 10) amplify a plain bf16 rounding of dS past the
+// gradient tolerance.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const uint32_t b0 = __float_as_uint(x0) & 0xFFFF0000u;
+  const uint32_t b1 = __float_as_uint(x1) & 0xFFFF0000u;
+  hi = __byte_perm(b0, b1, 0x7632);
+  lo = pack_bf16x2(x0 - __uint_as_float(b0), x1 - __uint_as_float(b1));
+}
+
+// ------------------------------------------------------------------ preprocess
+// D_i = sum_c dO_ic O_ic.  d/8 threads per row, 8 elements per thread; the
+// loop bound is uniform across a warp so every lane reaches the shuffles.
+template <int D>
+__global__ void __launch_bounds__(256) preprocess_kernel(const float* __restrict__ o,
+                                                         const uint16_t* __restrict__ dout,
+                                                         float* __restrict__ delta, const int rows) {
+  constexpr int G = D / 8;            // threads per row
+  constexpr int kRowsPerWarp = 32 / G;
+  const int sub = threadIdx.x % G;
+  const int gi = (threadIdx.x & 31) / G;
+  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (int base = warp_global * kRowsPerWarp; base < rows; base += nwarps * kRowsPerWarp) {
+    const int row = base + gi;
+    float acc = 0.f;
+    if (row < rows) {
+      const float4* op = reinterpret_cast<const float4*>(o + static_cast<size_t>(row) * D) + 2 * sub;
+      const uint4 h = __ldg(reinterpret_cast<const uint4*>(dout + static_cast<size_t>(row) * D) + sub);
+      const float4 a = __ldg(op);
+      const float4 b = __ldg(op + 1);
+      acc = a.x * bf16_bits_to_float(h.x & 0xFFFFu) + a.y * bf16_bits_to_float(h.x >> 16) +
+            a.z * bf16_bits_to_float(h.y & 0xFFFFu) + a.w * bf16_bits_to_float(h.y >> 16) +
+            b.x * bf16_bits_to_float(h.z & 0xFFFFu) + b.y * bf16_bits_to_float(h.z >> 16) +
+            b.z * bf16_bits_to_float(h.w & 0xFFFFu) + b.w * bf16_bits_to_float(h.w >> 16);
+    }
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (sub == 0 && row < rows) delta[row] = acc;
+  }
+}
+
+// ------------------------------------------------------------------ dK / dV
+
+template <int D>
+struct KvLayout {
+  static constexpr int kTileBytes = kTileRows * D * 2;
+  static constexpr int kStages = (D == 128) ? 2 : 4;  // (Q, dO) ring
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kTileBytes;
+  static constexpr int kQdOff = 2 * kTileBytes;             // stage s: Q at +0, dO at +kTileBytes
+  static constexpr int kLdOff = kQdOff + kStages * 2 * kTileBytes;  // stage s: lse2[128], d[128]
+  static constexpr int kBarOff = kLdOff + kStages * 1024;
+  static constexpr int KV_FULL = 0;
+  static constexpr int KV_EMPTY = 1;
+  static constexpr int QD_FULL = 2;
+  static constexpr int QD_EMPTY = QD_FULL + kStages;
+  static constexpr int LD_FULL = QD_EMPTY + kStages;
+  static constexpr int LD_EMPTY = LD_FULL + kStages;
+  static constexpr int SDP_FULL = LD_EMPTY + kStages;
+  static constexpr int PDS_FULL = SDP_FULL + 1;
+  static constexpr int ACC_FULL = PDS_FULL + 1;
+  static constexpr int DRAIN = ACC_FULL + 1;
+  static constexpr int kNumBars = DRAIN + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  // tensor memory columns
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+};
+
+constexpr int kKvThreads = 352;  // 8 elementwise warps, TMA, MMA, LSE/D loader
+
+// Query tiles that see key tile j.
+__device__ __forceinline__ void kv_range(int j, int nt, bool causal, int& i0, int& i1) {
+  i0 = causal ? j : 0;
+  i1 = nt;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kKvThreads, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const float* __restrict__ lse, const float* __restrict__ delta, float* __restrict__ dk,
+                float* __restrict__ dv, const int n, const float scale, const float scale_log2,
+                const SchedParams sp, int* status, const unsigned long long limit_ns) {
+  using L = KvLayout<D>;
+  constexpr int S = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + L::kBarOff;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bars + 8 * L::KV_FULL, 1);
+    mbar_init(bars + 8 * L::KV_EMPTY, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bars + 8 * (L::QD_FULL + s), 1);
+      mbar_init(bars + 8 * (L::QD_EMPTY + s), 1);
+      mbar_init(bars + 8 * (L::LD_FULL + s), 32);
+      mbar_init(bars + 8 * (L::LD_EMPTY + s), 256);
+    }
+    mbar_init(bars + 8 * L::SDP_FULL, 1);
+    mbar_init(bars + 8 * L::PDS_FULL, 256);
+    mbar_init(bars + 8 * L::ACC_FULL, 1);
+    mbar_init(bars + 8 * L::DRAIN, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, status, limit_ns};
+  const int nt = (n + kTileRows - 1) / kTileRows;
+  auto BAR = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+
+  if (warp < 8) {
+    // ------------------------------------------------ P^T and dS^T (thread = key row)
+    const int w = warp >> 2;  // warpgroup: query columns [64 w, 64 w + 64)
+    const int r = ((warp & 3) << 5) + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    const float* ld_base = reinterpret_cast<const float*>(smem + L::kLdOff);
+    uint32_t ldn = 0, sn = 0, an = 0;
+    SchedIter it = sched_begin(sp);
+    int head, j;
+    bool ok = true;
+    while (ok && sched_next(it, sp, blockIdx.x, head, j)) {
+      int i0, i1;
+      kv_range(j, nt, CAUSAL, i0, i1);
+      const int unit = head * sp.units_per_head + j;
+      for (int i = i0; i < i1; ++i) {
+        const uint32_t ls = ldn % S;
+        ok = warp_wait(BAR(L::LD_FULL + ls), (ldn / S) & 1, wc, SITE_KV_EW_LD, unit);
+        if (!ok) break;
+        ok = warp_wait(BAR(L::SDP_FULL), sn & 1, wc, SITE_KV_EW_SDP, unit);
+        if (!ok) break;
+        ++sn;
+        tc_fence_after();
+        const float* l2s = ld_base + ls * 256;
+        const float* dds = l2s + 128;
+        const bool diag = CAUSAL && (i == j);
+        // P^T and dS^T for 32 query columns starting at col0; P packed into pk,
+        // dS split into hk (hi) and lk (lo)
+        auto chunk = [&](const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&pk)[16],
+                         uint32_t (&hk)[16], uint32_t (&lk)[16]) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(l2s + col0 + c);
+            const float4 d4 = *reinterpret_cast<const float4*>(dds + col0 + c);
+            const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+            float p[4], ds[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float pe = ex2_approx(fmaf(__uint_as_float(sr[c + e]), scale_log2, -la[e]));
+              if (diag && (col0 + c + e) < r) pe = 0.f;  // query before key: masked
+              p[e] = pe;
+              ds[e] = pe * (__uint_as_float(dr[c + e]) - da[e]);
+            }
+            pk[c / 2] = pack_bf16x2(p[0], p[1]);
+            pk[c / 2 + 1] = pack_bf16x2(p[2], p[3]);
+            split_bf16x2(ds[0], ds[1], hk[c / 2], lk[c / 2]);
+            split_bf16x2(ds[2], ds[3], hk[c / 2 + 1], lk[c / 2 + 1]);
+          }
+        };
+        // Column slice of this warpgroup: S^T [64w, 64w+64), dP^T likewise.
+        // After use the slice holds P^T in S cols [64w, 64w+32), dS^T lo in
+        // S cols [64w+32, 64w+64) and dS^T hi in dP cols [64w, 64w+32); every
+        // store lands on columns this thread has already read.
+        const uint32_t tS = tmem + lane_off + L::kColS + 64 * w;
+        const uint32_t tD = tmem + lane_off + L::kColDP + 64 * w;
+        {
+          uint32_t s0[32], s1[32], d0[32], pk[16], hk[16], lk[16];
+          tmem_ld32(tS, s0);
+          tmem_ld32(tS + 32, s1);
+          tmem_ld32(tD, d0);
+          tmem_ld_wait();
+          chunk(s0, d0, 64 * w, pk, hk, lk);
+          tmem_st16(tS, pk);
+          tmem_st16(tD, hk);
+          tmem_st16(tS + 32, lk);
+          uint32_t d1[32];
+          tmem_ld32(tD + 32, d1);
+          tmem_ld_wait();
+          chunk(s1, d1, 64 * w + 32, pk, hk, lk);
+          tmem_st16(tS + 16, pk);
+          tmem_st16(tD + 16, hk);
+          tmem_st16(tS + 48, lk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR(L::PDS_FULL));
+        mbar_arrive(BAR(L::LD_EMPTY + ls));
+        ++ldn;
+      }
+      if (!ok) break;
+      // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
+      ok = warp_wait(BAR(L::ACC_FULL), an & 1, wc, SITE_KV_EW_ACC, unit);
+      if (!ok) break;
+      ++an;
+      tc_fence_after();
+      const int row = j * kTileRows + r;
+      const bool valid = row < n;
+      float* dst = (w == 0 ? dv : dk) + (static_cast<size_t>(head) * n + row) * D;
+      const uint32_t col = (w == 0) ? L::kColDV : L::kColDK;
+      const float mul = (w == 0) ? 1.0f : scale;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + col + 32 * c, v);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float4 o4;
+            o4.x = __uint_as_float(v[4 * e + 0]) * mul;
+            o4.y = __uint_as_float(v[4 * e + 1]) * mul;
+            o4.z = __uint_as_float(v[4 * e + 2]) * mul;
+            o4.w = __uint_as_float(v[4 * e + 3]) * mul;
+            *reinterpret_cast<float4*>(dst + 32 * c + 4 * e) = o4;
+          }
+        }
+      }
+    }
+  } else if (warp == 8) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_keep = l2_policy_evict_last();
+      const uint64_t pol_once = l2_policy_evict_first();
+      uint32_t kvn = 0, qdpos = 0;
+      SchedIter it = sched_begin(sp);
+      int head, j;
+      bool ok = true;
+      while (ok && sched_next(it, sp, blockIdx.x, head, j)) {
+        int i0, i1;
+        kv_range(j, nt, CAUSAL, i0, i1);
+        const int unit = head * sp.units_per_head + j;
+        ok = wait_bounded(BAR(L::KV_EMPTY), (kvn & 1) ^ 1, wc, SITE_KV_LOAD_KV, unit);
+        if (!ok) break;
+        ++kvn;
+        mbar_arrive_expect_tx(BAR(L::KV_FULL), 2 * L::kTileBytes);
+#pragma unroll
+        for (int kb = 0; kb < D / 64; ++kb) {
+          tma_load_3d_hint(sbase + L::kKOff + kb * 16384, &tm_k, BAR(L::KV_FULL), kb * 64, j * kTileRows, head,
+                           pol_once);
+          tma_load_3d_hint(sbase + L::kVOff + kb * 16384, &tm_v, BAR(L::KV_FULL), kb * 64, j * kTileRows, head,
+                           pol_once);
+        }
+        for (int i = i0; i < i1; ++i) {
+          const uint32_t s = qdpos % S, use = qdpos / S;
+          ok = wait_bounded(BAR(L::QD_EMPTY + s), (use & 1) ^ 1, wc, SITE_KV_LOAD_QD, unit);
+          if (!ok) break;
+          mbar_arrive_expect_tx(BAR(L::QD_FULL + s), 2 * L::kTileBytes);
+          const uint32_t qa = sbase + L::kQdOff + s * 2 * L::kTileBytes;
+#pragma unroll
+          for (int kb = 0; kb < D / 64; ++kb) {
+            tma_load_3d_hint(qa + kb * 16384, &tm_q, BAR(L::QD_FULL + s), kb * 64, i * kTileRows, head, pol_keep);
+            tma_load_3d_hint(qa + L::kTileBytes + kb * 16384, &tm_do, BAR(L::QD_FULL + s), kb * 64, i * kTileRows,
+                             head, pol_keep);
+          }
+          ++qdpos;
+        }
+      }
+      if (!ok) {
+        if (kvn > 0) drain_wait(BAR(L::KV_FULL), (kvn - 1) & 1, limit_ns);
+        for (uint32_t s = 0; s < static_cast<uint32_t>(S); ++s) {
+          if (qdpos > s) {
+            const uint32_t last = qdpos - 1 - ((qdpos - 1 - s) % S);
+            drain_wait(BAR(L::QD_FULL + s), (last / S) & 1, limit_ns);
+          }
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
+      uint32_t kvn = 0, qdpos = 0, pn = 0;
+      SchedIter it = sched_begin(sp);
+      int head, j;
+      bool ok = true;
+      while (ok && sched_next(it, sp, blockIdx.x, head, j)) {
+        int i0, i1;
+        kv_range(j, nt, CAUSAL, i0, i1);
+        const int unit = head * sp.units_per_head + j;
+        ok = wait_bounded(BAR(L::KV_FULL), kvn & 1, wc, SITE_KV_MMA_KV, unit);
+        if (!ok) break;
+        ++kvn;
+        for (int i = i0; i < i1; ++i) {
+          const uint32_t s = qdpos % S;
+          ok = wait_bounded(BAR(L::QD_FULL + s), (qdpos / S) & 1, wc, SITE_KV_MMA_QD, unit);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t qa = sbase + L::kQdOff + s * 2 * L::kTileBytes;
+          const uint32_t da = qa + L::kTileBytes;
+          // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = 128 queries, K = d
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            umma_ss(tmem + L::kColS, sdesc_sw128(sbase + L::kKOff + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
+                    id_s, ks > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            umma_ss(tmem + L::kColDP, sdesc_sw128(sbase + L::kVOff + off, 16, 1024),
+                    sdesc_sw128(da + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(BAR(L::SDP_FULL));
+          ok = wait_bounded(BAR(L::PDS_FULL), pn & 1, wc, SITE_KV_MMA_PDS, unit);
+          if (!ok) break;
+          ++pn;
+          tc_fence_after();
+          // dV += P^T dO and dK += dS^T Q: M = 128 keys, N = d, K = 128 queries.
+          // P^T / dS^T of queries [64 w, 64 w + 64) sit in the first 32 columns of
+          // the warpgroup's 64-column slice.
+          const bool first = (i == i0);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
+            umma_ts(tmem + L::kColDV, tmem + L::kColS + acol, sdesc_sw128(da + ks * 2048, kTileRows * 128, 1024),
+                    id_acc, (!first || ks > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
+            umma_ts(tmem + L::kColDK, tmem + L::kColDP + acol, sdesc_sw128(qa + ks * 2048, kTileRows * 128, 1024),
+                    id_acc, (!first || ks > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {  // dS^T lo part
+            const uint32_t acol = 32 + 64 * (ks >> 2) + 8 * (ks & 3);
+            umma_ts(tmem + L::kColDK, tmem + L::kColS + acol, sdesc_sw128(qa + ks * 2048, kTileRows * 128, 1024),
+                    id_acc, 1u);
+          }
+          umma_commit(BAR(L::QD_EMPTY + s));
+          ++qdpos;
+        }
+        if (!ok) break;
+        umma_commit(BAR(L::ACC_FULL));
+        umma_commit(BAR(L::KV_EMPTY));
+      }
+      umma_commit(BAR(L::DRAIN));
+      drain_wait(BAR(L::DRAIN), 0, limit_ns);
+    }
+  } else {
+    // ------------------------------------------- LSE / D rows of each query tile
+    const float* lse_h = nullptr;
+    uint32_t ldn = 0;
+    float* ld_base = reinterpret_cast<float*>(smem + L::kLdOff);
+    SchedIter it = sched_begin(sp);
+    int head, j;
+    bool ok = true;
+    while (ok && sched_next(it, sp, blockIdx.x, head, j)) {
+      int i0, i1;
+      kv_range(j, nt, CAUSAL, i0, i1);
+      const int unit = head * sp.units_per_head + j;
+      lse_h = lse + static_cast<size_t>(head) * n;
+      const float* d_h = delta + static_cast<size_t>(head) * n;
+      for (int i = i0; i < i1; ++i) {
+        const uint32_t ls = ldn % S;
+        ok = warp_wait(BAR(L::LD_EMPTY + ls), ((ldn / S) & 1) ^ 1, wc, SITE_KV_LD_EMPTY, unit);
+        if (!ok) break;
+        float* l2s = ld_base + ls * 256;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int idx = lane * 4 + t;
+          const int q = i * kTileRows + idx;
+          const bool in = q < n;
+          l2s[idx] = in ? lse_h[q] * kLog2e : CUDART_INF_F;
+          l2s[128 + idx] = in ? d_h[q] : 0.f;
+        }
+        mbar_arrive(BAR(L::LD_FULL + ls));
+        ++ldn;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ dQ
+
+template <int D>
+struct QLayout {
+  static constexpr int kTileBytes = kTileRows * D * 2;
+  static constexpr int kStages = (D == 128) ? 2 : 4;  // (K, V) ring
+  static constexpr int kQOff = 0;
+  static constexpr int kDoOff = kTileBytes;
+  static constexpr int kKvOff = 2 * kTileBytes;  // stage s: K at +0, V at +kTileBytes
+  static constexpr int kXchOff = kKvOff + kStages * 2 * kTileBytes;  // [2 units][2 warpgroups][128] fp32
+  static constexpr int kBarOff = kXchOff + 2 * 2 * 128 * 4;
+  static constexpr int Q_FULL = 0;
+  static constexpr int Q_EMPTY = 1;
+  static constexpr int KV_FULL = 2;
+  static constexpr int KV_EMPTY = KV_FULL + kStages;
+  static constexpr int SDP_FULL = KV_EMPTY + kStages;
+  static constexpr int DS_FULL = SDP_FULL + 1;
+  static constexpr int ACC_FULL = DS_FULL + 1;
+  static constexpr int XCH = ACC_FULL + 1;
+  static constexpr int DRAIN = XCH + 1;
+  static constexpr int kNumBars = DRAIN + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  // S [0,128): after use P (bf16) in each warpgroup's first 32 columns and
+  // dS lo in its last 32; dP [128,256): dS hi in each warpgroup's first 32;
+  // dQ accumulator [256, 256+d); B = sum_j P_ij k_j accumulator [256+d, 256+2d).
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColB = 256 + D;
+};
+
+constexpr int kQThreads = 320;  // 8 elementwise warps, TMA, MMA
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kQThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+              const float* __restrict__ lse, float* __restrict__ delta, float* __restrict__ dq, const int n,
+              const float scale, const float scale_log2, const SchedParams sp, int* status,
+              const unsigned long long limit_ns) {
+  using L = QLayout<D>;
+  constexpr int S = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + L::kBarOff;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bars + 8 * L::Q_FULL, 1);
+    mbar_init(bars + 8 * L::Q_EMPTY, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bars + 8 * (L::KV_FULL + s), 1);
+      mbar_init(bars + 8 * (L::KV_EMPTY + s), 1);
+    }
+    mbar_init(bars + 8 * L::SDP_FULL, 1);
+    mbar_init(bars + 8 * L::DS_FULL, 256);
+    mbar_init(bars + 8 * L::ACC_FULL, 1);
+    mbar_init(bars + 8 * L::XCH, 256);
+    mbar_init(bars + 8 * L::DRAIN, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, status, limit_ns};
+  const int nt = (n + kTileRows - 1) / kTileRows;
+  auto BAR = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+
+  if (warp < 8) {
+    // ------------------------------------------------- dS (thread = query row)
+    // The row term comes in as D'_i = rowsum(dO o O) with O from the forward
+    // pass, whose P was rounded to bf16 for the PV product.  The kernel sees
+    // every key of its rows, so it also sums delta_i = sum_j dS'_ij =
+    // sum_j P_ij dP_ij - D'_i in fp32, corrects its own product with
+    // dQ = scale (sum_j dS'_ij k_j - delta_i sum_j P_ij k_j), and stores the
+    // corrected D_i = D'_i + delta_i for the dK/dV kernel.
+    const int w = warp >> 2;  // key columns [64 w, 64 w + 64)
+    const int r = ((warp & 3) << 5) + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
+    float* xch = reinterpret_cast<float*>(smem + L::kXchOff);
+    uint32_t sn = 0, an = 0;
+    SchedIter it = sched_begin(sp);
+    int head, i;
+    bool ok = true;
+    while (ok && sched_next(it, sp, blockIdx.x, head, i)) {
+      const int nk = CAUSAL ? min(i + 1, nt) : nt;
+      const int unit = head * sp.units_per_head + i;
+      const int row = i * kTileRows + r;
+      const bool valid = row < n;
+      const float l2 = valid ? lse[static_cast<size_t>(head) * n + row] * kLog2e : CUDART_INF_F;
+      const float dd = valid ? delta[static_cast<size_t>(head) * n + row] : 0.f;
+      const float nl2 = -l2;
+      float dsum = 0.f;  // this warpgroup's share of delta_i
+      for (int jt = 0; jt < nk; ++jt) {
+        ok = warp_wait(BAR(L::SDP_FULL), sn & 1, wc, SITE_Q_EW_SDP, unit);
+        if (!ok) break;
+        ++sn;
+        tc_fence_after();
+        const bool diag = CAUSAL && (jt == i);
+        const bool tail = (jt == nt - 1) && ((n & (kTileRows - 1)) != 0);
+        // number of eligible key columns of this tile for this row
+        const int lim = (diag || tail) ? ((CAUSAL ? min(row + 1, n) : n) - jt * kTileRows) : kTileRows;
+        auto chunk = [&](const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&pk)[16],
+                         uint32_t (&hk)[16], uint32_t (&lk)[16]) {
+          float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, nl2));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), scale_log2, nl2));
+            if (col0 + c >= lim) p0 = 0.f;
+            if (col0 + c + 1 >= lim) p1 = 0.f;
+            const float ds0 = p0 * (__uint_as_float(dr[c]) - dd);
+            const float ds1 = p1 * (__uint_as_float(dr[c + 1]) - dd);
+            acc0 += ds0;
+            acc1 += ds1;
+            pk[c / 2] = pack_bf16x2(p0, p1);
+            split_bf16x2(ds0, ds1, hk[c / 2], lk[c / 2]);
+          }
+          dsum += acc0 + acc1;
+        };
+        // Each store lands on columns this thread has already read.
+        const uint32_t tS = tmem + lane_off + L::kColS + 64 * w;
+        const uint32_t tD = tmem + lane_off + L::kColDP + 64 * w;
+        {
+          uint32_t s0[32], s1[32], d0[32], pk[16], hk[16], lk[16];
+          tmem_ld32(tS, s0);
+          tmem_ld32(tS + 32, s1);
+          tmem_ld32(tD, d0);
+          tmem_ld_wait();
+          chunk(s0, d0, 64 * w, pk, hk, lk);
+          tmem_st16(tS, pk);
+          tmem_st16(tD, hk);
+          tmem_st16(tS + 32, lk);
+          uint32_t d1[32];
+          tmem_ld32(tD + 32, d1);
+          tmem_ld_wait();
+          chunk(s1, d1, 64 * w + 32, pk, hk, lk);
+          tmem_st16(tS + 16, pk);
+          tmem_st16(tD + 16, hk);
+          tmem_st16(tS + 48, lk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR(L::DS_FULL));
+      }
+      if (!ok) break;
+      // combine the two warpgroups' halves of delta_i (slots alternate by unit)
+      float* slot = xch + (an & 1) * 256;
+      slot[w * 128 + r] = dsum;
+      mbar_arrive(BAR(L::XCH));
+      ok = warp_wait(BAR(L::XCH), an & 1, wc, SITE_Q_EW_XCH, unit);
+      if (!ok) break;
+      const float dlt = slot[r] + slot[128 + r];
+      ok = warp_wait(BAR(L::ACC_FULL), an & 1, wc, SITE_Q_EW_ACC, unit);
+      if (!ok) break;
+      ++an;
+      tc_fence_after();
+      if (w == 0 && valid) delta[static_cast<size_t>(head) * n + row] = dd + dlt;
+      // warpgroup w writes dQ columns [w d/2, (w+1) d/2)
+      float* dst = dq + (static_cast<size_t>(head) * n + row) * D;
+#pragma unroll 1
+      for (int c = w * (D / 64); c < (w + 1) * (D / 64); ++c) {
+        uint32_t v[32], bv[32];
+        tmem_ld32(tmem + lane_off + L::kColDQ + 32 * c, v);
+        tmem_ld32(tmem + lane_off + L::kColB + 32 * c, bv);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float4 o4;
+            o4.x = (__uint_as_float(v[4 * e + 0]) - dlt * __uint_as_float(bv[4 * e + 0])) * scale;
+            o4.y = (__uint_as_float(v[4 * e + 1]) - dlt * __uint_as_float(bv[4 * e + 1])) * scale;
+            o4.z = (__uint_as_float(v[4 * e + 2]) - dlt * __uint_as_float(bv[4 * e + 2])) * scale;
+            o4.w = (__uint_as_float(v[4 * e + 3]) - dlt * __uint_as_float(bv[4 * e + 3])) * scale;
+            *reinterpret_cast<float4*>(dst + 32 * c + 4 * e) = o4;
+          }
+        }
+      }
+    }
+  } else if (warp == 8) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_keep = l2_policy_evict_last();
+      const uint64_t pol_once = l2_policy_evict_first();
+      uint32_t qn = 0, kvpos = 0;
+      SchedIter it = sched_begin(sp);
+      int head, i;
+      bool ok = true;
+      while (ok && sched_next(it, sp, blockIdx.x, head, i)) {
+        const int nk = CAUSAL ? min(i + 1, nt) : nt;
+        const int unit = head * sp.units_per_head + i;
+        ok = wait_bounded(BAR(L::Q_EMPTY), (qn & 1) ^ 1, wc, SITE_Q_LOAD_Q, unit);
+        if (!ok) break;
+        ++qn;
+        mbar_arrive_expect_tx(BAR(L::Q_FULL), 2 * L::kTileBytes);
+#pragma unroll
+        for (int kb = 0; kb < D / 64; ++kb) {
+          tma_load_3d_hint(sbase + L::kQOff + kb * 16384, &tm_q, BAR(L::Q_FULL), kb * 64, i * kTileRows, head,
+                           pol_once);
+          tma_load_3d_hint(sbase + L::kDoOff + kb * 16384, &tm_do, BAR(L::Q_FULL), kb * 64, i * kTileRows, head,
+                           pol_once);
+        }
+        for (int jt = 0; jt < nk; ++jt) {
+          const uint32_t s = kvpos % S, use = kvpos / S;
+          ok = wait_bounded(BAR(L::KV_EMPTY + s), (use & 1) ^ 1, wc, SITE_Q_LOAD_KV, unit);
+          if (!ok) break;
+          mbar_arrive_expect_tx(BAR(L::KV_FULL + s), 2 * L::kTileBytes);
+          const uint32_t ka = sbase + L::kKvOff + s * 2 * L::kTileBytes;
+#pragma unroll
+          for (int kb = 0; kb < D / 64; ++kb) {
+            tma_load_3d_hint(ka + kb * 16384, &tm_k, BAR(L::KV_FULL + s), kb * 64, jt * kTileRows, head, pol_keep);
+            tma_load_3d_hint(ka + L::kTileBytes + kb * 16384, &tm_v, BAR(L::KV_FULL + s), kb * 64, jt * kTileRows,
+                             head, pol_keep);
+          }
+          ++kvpos;
+        }
+      }
+      if (!ok) {
+        if (qn > 0) drain_wait(BAR(L::Q_FULL), (qn - 1) & 1, limit_ns);
+        for (uint32_t s = 0; s < static_cast<uint32_t>(S); ++s) {
+          if (kvpos > s) {
+            const uint32_t last = kvpos - 1 - ((kvpos - 1 - s) % S);
+            drain_wait(BAR(L::KV_FULL + s), (last / S) & 1, limit_ns);
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
+      uint32_t qn = 0, kvpos = 0, dn = 0;
+      SchedIter it = sched_begin(sp);
+      int head, i;
+      bool ok = true;
+      while (ok && sched_next(it, sp, blockIdx.x, head, i)) {
+        const int nk = CAUSAL ? min(i + 1, nt) : nt;
+        const int unit = head * sp.units_per_head + i;
+        ok = wait_bounded(BAR(L::Q_FULL), qn & 1, wc, SITE_Q_MMA_Q, unit);
+        if (!ok) break;
+        ++qn;
+        for (int jt = 0; jt < nk; ++jt) {
+          const uint32_t s = kvpos % S;
+          ok = wait_bounded(BAR(L::KV_FULL + s), (kvpos / S) & 1, wc, SITE_Q_MMA_KV, unit);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t ka = sbase + L::kKvOff + s * 2 * L::kTileBytes;
+          const uint32_t va = ka + L::kTileBytes;
+          // S = Q K^T and dP = dO V^T: M = 128 queries, N = 128 keys, K = d
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            umma_ss(tmem + L::kColS, sdesc_sw128(sbase + L::kQOff + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                    id_s, ks > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            umma_ss(tmem + L::kColDP, sdesc_sw128(sbase + L::kDoOff + off, 16, 1024),
+                    sdesc_sw128(va + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(BAR(L::SDP_FULL));
+          ok = wait_bounded(BAR(L::DS_FULL), dn & 1, wc, SITE_Q_MMA_DS, unit);
+          if (!ok) break;
+          ++dn;
+          tc_fence_after();
+          // dQ += dS K: M = 128 queries, N = d, K = 128 keys; K tile MN-major
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
+            umma_ts(tmem + L::kColDQ, tmem + L::kColDP + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
+                    id_acc, (jt > 0 || ks > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {  // dS lo part
+            const uint32_t acol = 32 + 64 * (ks >> 2) + 8 * (ks & 3);
+            umma_ts(tmem + L::kColDQ, tmem + L::kColS + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
+                    id_acc, 1u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {  // B += P K, for the delta correction
+            const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
+            umma_ts(tmem + L::kColB, tmem + L::kColS + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
+                    id_acc, (jt > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(BAR(L::KV_EMPTY + s));
+          ++kvpos;
+        }
+        if (!ok) break;
+        umma_commit(BAR(L::ACC_FULL));
+        umma_commit(BAR(L::Q_EMPTY));
+      }
+      umma_commit(BAR(L::DRAIN));
+      drain_wait(BAR(L::DRAIN), 0, limit_ns);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+  const int rows = a.heads * a.n;
+  preprocess_kernel<D><<<a.grid_pre, 256, 0, stream>>>(a.o, a.dout, a.delta, rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  {
+    // dQ first: it turns D' = rowsum(dO o O) into the exact row term
+    using L = QLayout<D>;
+    auto kern = dq_kernel<D, CAUSAL>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<a.grid_q, kQThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dq,
+                                                         a.n, a.scale, a.scale_log2, a.sched_q, a.status,
+                                                         a.wait_limit_ns);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    using L = KvLayout<D>;
+    auto kern = dkdv_kernel<D, CAUSAL>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<a.grid_kv, kKvThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dk,
+                                                           a.dv, a.n, a.scale, a.scale_log2, a.sched_kv, a.status,
+                                                           a.wait_limit_ns);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
+  return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+}
 
 }  // namespace fa

@@ -1,8 +1,10 @@
 // Persistent tile scheduler shared by the kernels and by host-side tests.
 //
-// Work unit: one head (b, h) and one pair of 128-row query tiles
-// (rows [256 p, 256 p + 256)).  Under the causal mask query tile t sweeps key
-// tiles 0..t, so unit p costs about 4p + 3 tile products: the work is
+// Work unit: one head (b, h) and one block index p along the sequence (for
+// the forward pass a pair of 128-row query tiles, rows [256 p, 256 p + 256);
+// for the backward kernels a single 128-row tile).  Under the causal mask
+// query tile t sweeps key tiles 0..t, so a forward unit costs about 4p + 3
+// tile products and the cost of a unit grows or shrinks with p: the work is
 // parallel over heads and over the query sequence, the partitioning the
 // FlashAttention-2 discussion on the FlashAttention Interview Questions page
 // ("What changed in FlashAttention-2 ...") credits for the speedup.
@@ -35,6 +37,7 @@ struct SchedParams {
   int group_heads;     // heads per L2 group
   int grid;            // persistent CTAs
   int causal;
+  int cost_grows;      // causal only: 1 if a unit's cost grows with its index p
 };
 
 struct SchedIter {
@@ -78,7 +81,7 @@ FA_HD bool sched_next(SchedIter& it, const SchedParams& p, int cta, int& head, i
       if (r < it.gsize) {
         const int level = r / it.hs;
         head = it.g * p.group_heads + (r - level * it.hs);
-        pair = p.causal ? (p.units_per_head - 1 - level) : level;
+        pair = (p.causal && p.cost_grows) ? (p.units_per_head - 1 - level) : level;
         return true;
       }
     }

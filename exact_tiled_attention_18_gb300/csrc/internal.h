@@ -42,6 +42,7 @@ struct BwdArgs {
   float scale_log2;
   int grid_kv;                          // CTAs of the dK/dV kernel
   int grid_q;                           // CTAs of the dQ kernel
+  int grid_pre;                         // CTAs of the preprocess kernel
   SchedParams sched_kv;
   SchedParams sched_q;
   int* status;

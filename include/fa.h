@@ -88,7 +88,9 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, float* o, float* l
  *   o, lse      : fp32 outputs of fa_fwd for the same q, k, v, scale, causal.
  *   dq, dk, dv  : fp32 [B][H][N][d], overwritten with dL/dQ, dL/dK, dL/dV.
  *   workspace   : fp32 buffer of fa_bwd_workspace_bytes(B, H, N) bytes that
- *                 receives D_i = sum_c dO_ic O_ic; or NULL, in which case the
+ *                 receives the row term D_i = sum_j P_ij dP_ij (first as
+ *                 rowsum(dO o O), then corrected to the probabilities the
+ *                 backward pass recomputes); or NULL, in which case the
  *                 library takes a stream-ordered allocation and frees it on
  *                 the same stream.
  * Computes P_ij = exp(s_ij - LSE_i), dV = P^T dO, dP = dO V^T,

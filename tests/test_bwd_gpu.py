@@ -1,0 +1,104 @@
+"""Backward parity: dQ, dK, dV (and D) from the CUDA path against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import exact_tiled_attention_18_gb300 as fa
+import oracle
+from exact_tiled_attention_18_gb300 import workloads
+from tests.helpers import GRAD_MAX_ABS, scale_for, to64
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_fwd_bwd(inp, causal, scale, workspace=True):
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    B, H, N, d = q.shape
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N) // 4, dtype=torch.float32, device="cuda") if workspace else None
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale, workspace=ws)
+    fa.sync_status()
+    return dq.cpu(), dk.cpu(), dv.cpu(), (ws.cpu() if ws is not None else None)
+
+
+def check_grads(got, ref, what, heads=None):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        g = g.numpy().astype(np.float64)
+        if heads is not None:
+            g = g[heads]
+        assert np.all(np.isfinite(g)), f"{what} {name}: non-finite"
+        err = np.abs(g - r).max()
+        assert err <= GRAD_MAX_ABS, f"{what} {name}: max abs {err:.3e}"
+
+
+SMALL = [
+    (1, 1, 256, 64, False),
+    (1, 1, 256, 64, True),
+    (1, 1, 1, 64, True),
+    (1, 1, 1, 128, False),
+    (1, 1, 127, 128, True),
+    (2, 1, 129, 128, False),
+    (1, 2, 200, 64, True),
+    (1, 1, 257, 128, True),
+    (1, 2, 300, 64, False),
+    (2, 2, 384, 128, True),
+    (1, 3, 517, 128, True),
+    (1, 2, 1000, 64, True),
+    (1, 1, 1024, 128, False),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", SMALL)
+def test_backward_small_matches_oracle(B, H, N, d, causal):
+    inp = workloads.make_inputs(B, H, N, d, seed=100 + N + d + causal, with_grad=True)
+    scale = scale_for(d)
+    dq, dk, dv, ws = gpu_fwd_bwd(inp, causal, scale)
+    x = {n: to64(inp[n]) for n in inp}
+    rq, rk, rv, rd = oracle.backward(x["q"], x["k"], x["v"], x["do"], scale, causal)
+    check_grads((dq, dk, dv), (rq, rk, rv), f"{(B, H, N, d, causal)}")
+    # D from the preprocess kernel (rowsum(dO o O), O from the forward kernel)
+    # against the oracle's sum_j P_ij dP_ij.  O carries at most the forward
+    # tolerance (1e-2 per element), so |dD_i| <= 1e-2 * sum_c |dO_ic|.
+    got_d = ws.numpy().reshape(B, H, N).astype(np.float64)
+    bound = 1e-2 * np.abs(x["do"]).sum(-1)
+    assert np.all(np.abs(got_d - rd) <= bound)
+
+
+def test_backward_without_workspace():
+    inp = workloads.make_inputs(1, 2, 333, 128, seed=9, with_grad=True)
+    scale = scale_for(128)
+    a = gpu_fwd_bwd(inp, True, scale, workspace=True)
+    b = gpu_fwd_bwd(inp, True, scale, workspace=False)
+    for x, y in zip(a[:3], b[:3]):
+        assert torch.equal(x, y)
+
+
+def test_gradient_sum_properties_full_size():
+    """At full size: sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i per head
+    (softmax rows sum to one; shifting every key by one vector changes nothing)."""
+    w = workloads.WORKLOADS["training_b4_h16_n8192_d128_causal"]
+    inp = workloads.workload_inputs(w, 0)
+    dq, dk, dv, _ = gpu_fwd_bwd(inp, w.causal, w.scale)
+    sum_dk = dk.double().sum(dim=2)
+    sum_dv = dv.double().sum(dim=2)
+    sum_do = inp["do"].double().sum(dim=2)
+    assert sum_dk.abs().max() < 0.5, sum_dk.abs().max()
+    assert (sum_dv - sum_do).abs().max() < 0.5, (sum_dv - sum_do).abs().max()
+
+
+@pytest.mark.parametrize("name,heads", [
+    ("training_b4_h16_n8192_d128_causal", [(0, 0), (3, 15)]),
+    ("long_context_b1_h32_n16384_d128_causal", [(0, 17)]),
+])
+def test_backward_full_size_whole_heads(name, heads):
+    """Full-size run in the bench's launch configuration; whole heads checked
+    against the oracle (heads are independent)."""
+    w = workloads.WORKLOADS[name]
+    inp = workloads.workload_inputs(w, 0)
+    dq, dk, dv, _ = gpu_fwd_bwd(inp, w.causal, w.scale)
+    for (b, h) in heads:
+        x = {n: to64(inp[n][b:b + 1, h:h + 1]) for n in inp}
+        rq, rk, rv, _ = oracle.backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal)
+        got = tuple(t[b:b + 1, h:h + 1] for t in (dq, dk, dv))
+        check_grads(got, (rq, rk, rv), f"{name} head {(b, h)}")
