@@ -48,6 +48,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd.restype = st
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd.restype = st
+        L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_bwd_noalloc.restype = st
         L.fa_bwd_workspace_bytes.argtypes = [i, i, i]
         L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.fa_sync_status.argtypes = [vp]
@@ -82,6 +84,16 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: 
 def fa_bwd(q: int, k: int, v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int, workspace: int,
            B: int, H: int, N: int, d: int, scale: float, causal: int, stream: int) -> int:
     return lib().fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, N, d, scale, causal, stream)
+
+
+def fa_bwd_noalloc(q: int, k: int, v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int,
+                   B: int, H: int, N: int, d: int, scale: float, causal: int, stream: int) -> int:
+    """Raw C call of the allocation-free backward (scratch held inside the
+    library, at most FA_NOALLOC_MAX_ROWS = B*H*N rows).  Returns the status."""
+    return lib().fa_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, scale, causal, stream)
+
+
+FA_NOALLOC_MAX_ROWS = 1 << 20
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> int:

@@ -100,6 +100,38 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const float* o, co
                  float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d, float scale,
                  int causal, fa_stream_t stream);
 
+/*
+ * Largest B*H*N that fa_bwd_noalloc accepts: 2^20 rows, i.e. 4 MiB of fp32
+ * scratch held in a static device array by every GPU that loads the library,
+ * for as long as the library stays loaded.
+ */
+#define FA_NOALLOC_MAX_ROWS (1 << 20)
+
+/*
+ * fa_bwd without any allocation.  The pages describe no such call: it exists
+ * for callers that cannot allocate device memory when they run the backward
+ * pass -- a host framework or inference runtime that owns every byte of
+ * device memory through its own pool and forbids libraries to allocate behind
+ * its back, or a latency-critical loop that reserved all memory up front and
+ * must not risk an allocation (or an out-of-memory failure) on its hot path.
+ *
+ * Arguments and results are those of fa_bwd, minus the workspace: the row
+ * term D lives in a fixed device array inside the library (see
+ * FA_NOALLOC_MAX_ROWS).  The call makes no cudaMalloc/cudaFree or other
+ * allocating call.  Its first call on a device looks up that array's device
+ * address (cudaGetSymbolAddress) with the caller's device current; make that
+ * first call before any stream capture on the device.
+ *
+ * Errors: as fa_bwd; B*H*N above FA_NOALLOC_MAX_ROWS returns
+ * FA_ERR_INVALID_ARG with nothing queued.  All calls on one device share the
+ * array, and it keeps the last call's contents (every call rewrites all of
+ * the rows it uses before reading them): two calls whose work overlaps on the
+ * GPU (different streams, not ordered) race on it and give wrong gradients.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                         const void* dO, float* dq, float* dk, float* dv, int B, int H, int N, int d, float scale,
+                         int causal, fa_stream_t stream);
+
 /* Bytes of the fa_bwd workspace: B*H*N fp32 values (0 on invalid sizes). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N);
 
