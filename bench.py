@@ -2,7 +2,8 @@
 """Attention TFLOP/s on GB300: forward + backward of exact tiled attention.
 
 One step is one pass of the whole path over one batch: fa_fwd (O, LSE) then
-fa_bwd (D preprocess, dK/dV, dQ).  Counted FLOPs: 4*B*H*N^2*d for the
+the three kernels of fa_bwd (D preprocess, dQ, dK/dV), each through its own
+C call so that each kernel is timed with CUDA events on the stream.  Counted FLOPs: 4*B*H*N^2*d for the
 forward, halved when causal, and 2.5x that for the backward.  Default
 workload: B=4, H=16, N=8192, d=128, causal, bf16 inputs ~ N(0,1).
 
@@ -63,20 +64,29 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_digest():
+KERNEL_SOURCES = {
+    "fwd_kernel": ["fwd.cu", "ptx.cuh", "fa_sched.h", "internal.h"],
+    "preprocess_kernel": ["bwd.cu", "ptx.cuh", "fa_sched.h", "internal.h"],
+    "dq_kernel": ["bwd.cu", "ptx.cuh", "fa_sched.h", "internal.h"],
+    "dkdv_kernel": ["bwd.cu", "ptx.cuh", "fa_sched.h", "internal.h"],
+}
+
+
+def kernel_source_digest(kernel):
+    """sha256 prefix of the source files a kernel is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_tiled_attention_18_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_tag):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    summary is missing or was taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary
+    (profiles/<kernel>_<workload>.md), or None when the summary is missing or
+    was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         with open(path) as f:
             text = f.read()
@@ -84,7 +94,7 @@ def ncu_traffic(kernel_tag):
         return None
     m_src = re.search(r"source_digest:\s*([0-9a-f]+)", text)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not m_src or not m_b or m_src.group(1) != kernel_source_digest():
+    if not m_src or not m_b or m_src.group(1) != kernel_source_digest(kernel):
         return None
     return float(m_b.group(1))
 
@@ -245,19 +255,23 @@ def run_ours(args):
     launches_per_step = 1 + (3 if do_bwd else 0)
 
     ev = []
+    nev = 5 if do_bwd else 2
 
     def step(record):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(nev)] if record else None
         if record:
-            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-            e0.record(stream)
+            e[0].record(stream)
         fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=(o, lse))
         if record:
-            e1.record(stream)
+            e[1].record(stream)
         if do_bwd:
-            fa.backward(q, k, v, o, lse, dout, causal=w.causal, scale=w.scale, workspace=ws, out=(dq, dk, dv))
+            # fa_bwd's three kernels, one C call each so each can be timed
+            for stage in range(3):
+                fa.backward_stage(stage, q, k, v, o, lse, dout, dq, dk, dv, ws, causal=w.causal, scale=w.scale)
+                if record:
+                    e[2 + stage].record(stream)
         if record:
-            e2.record(stream)
-            ev.append((e0, e1, e2))
+            ev.append(e)
 
     for _ in range(args.warmup):
         step(False)
@@ -279,8 +293,10 @@ def run_ours(args):
     fa.sync_status(device)
 
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, device)
-    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
-    bwd_ms = statistics.mean(b.elapsed_time(c) for _, b, c in ev) if do_bwd else 0.0
+    # per-kernel average duration over the timed steps
+    kern_ms = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev) for i in range(nev - 1)]
+    fwd_ms = kern_ms[0]
+    bwd_ms = sum(kern_ms[1:]) if do_bwd else 0.0
     ms_per_step = total_ms / args.steps
     step_flops = w.fwd_flops() + (w.bwd_flops() if do_bwd else 0.0)
     value = step_flops * world / (ms_per_step * 1e-3) / 1e12
@@ -332,17 +348,34 @@ def run_ours(args):
     burst = peaks["bf16_tflops"]
     fwd_tflops = w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
     bwd_tflops = w.bwd_flops() / (bwd_ms * 1e-3) / 1e12 if do_bwd else None
-    # dominant kernel: the one with the larger share of the step
-    if do_bwd and bwd_ms > fwd_ms:
-        dom = {"kernel": "fa_bwd (preprocess + dK/dV + dQ)", "ms": bwd_ms, "tflops": bwd_tflops,
-               "tag": f"bwd_kernels_{w.name}"}
+    # Algorithmic work per launch of each kernel (one launch covers the whole
+    # batch): forward 2 GEMMs (S, PV); dQ 3 (S, dP, dQ); dK/dV 4 (S, dP, dV,
+    # dK), each 2*N^2*d per head, halved under the causal mask; the
+    # preprocess moves dO (bf16) and O (fp32) in and D (fp32) out.
+    gemm = w.fwd_flops() / 2
+    rows = w.B * w.H * w.N
+    kernels = [("fwd_kernel", fwd_ms, "tensor", 2 * gemm)]
+    if do_bwd:
+        kernels += [("preprocess_kernel", kern_ms[1], "hbm", rows * (w.d * 6 + 4)),
+                    ("dq_kernel", kern_ms[2], "tensor", 3 * gemm),
+                    ("dkdv_kernel", kern_ms[3], "tensor", 4 * gemm)]
+    name, ms, bound, work = max(kernels, key=lambda t: t[1])
+    if bound == "tensor":
+        achieved, peak, unit = work / (ms * 1e-3) / 1e12, sustained, "TFLOP/s"
+        peak_kind = f"{peak_kind} bf16 sustained (kernel timed inside a long loop)"
     else:
-        dom = {"kernel": "fwd_kernel", "ms": fwd_ms, "tflops": fwd_tflops, "tag": f"fwd_kernel_{w.name}"}
-    roofline = {"bound": "tensor", "kernel": dom["kernel"], "achieved": round(dom["tflops"], 2),
-                "peak": sustained, "unit": "TFLOP/s", "frac": round(dom["tflops"] / sustained, 4),
-                "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long loop)",
-                "frac_of_burst_peak": round(dom["tflops"] / burst, 4),
-                "traffic": ncu_traffic(dom["tag"])}
+        achieved, peak, unit = work / (ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+        peak_kind = f"{peak_kind} HBM copy bandwidth"
+    roofline = {"bound": bound, "kernel": name, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                "algorithmic_per_launch": work, "ms_per_launch": round(ms, 4),
+                "traffic": ncu_traffic(name, w.name)}
+    if bound == "tensor":
+        roofline["frac_of_burst_peak"] = round(achieved / burst, 4)
+    per_kernel = {n: {"ms": round(t, 4),
+                      ("tflops" if b == "tensor" else "gbs"): round(wk / (t * 1e-3) / (1e12 if b == "tensor" else 1e9), 2),
+                      "share": round(t / sum(k[1] for k in kernels), 4)}
+                  for n, t, b, wk in kernels}
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -364,6 +397,7 @@ def run_ours(args):
                 "frac_of_sustained": round(fwd_tflops / sustained, 4), "frac_of_burst": round(fwd_tflops / burst, 4)},
         "bwd": ({"ms": round(bwd_ms, 4), "tflops": round(bwd_tflops, 2),
                  "frac_of_sustained": round(bwd_tflops / sustained, 4)} if do_bwd else None),
+        "kernels": per_kernel,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,

@@ -3,9 +3,11 @@
 from .binding import (  # noqa: F401
     FAError,
     backward,
+    backward_stage,
     FA_NOALLOC_MAX_ROWS,
     fa_bwd,
     fa_bwd_noalloc,
+    fa_bwd_stage,
     fa_bwd_workspace_bytes,
     fa_fwd,
     fa_last_failure,

@@ -48,6 +48,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd.restype = st
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd.restype = st
+        L.fa_bwd_stage.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_bwd_stage.restype = st
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd_noalloc.restype = st
         L.fa_bwd_workspace_bytes.argtypes = [i, i, i]
@@ -84,6 +86,12 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: 
 def fa_bwd(q: int, k: int, v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int, workspace: int,
            B: int, H: int, N: int, d: int, scale: float, causal: int, stream: int) -> int:
     return lib().fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, N, d, scale, causal, stream)
+
+
+def fa_bwd_stage(stage: int, q: int, k: int, v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int,
+                 workspace: int, B: int, H: int, N: int, d: int, scale: float, causal: int, stream: int) -> int:
+    """Raw C call of one backward stage (0 preprocess, 1 dQ, 2 dK/dV)."""
+    return lib().fa_bwd_stage(stage, q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, N, d, scale, causal, stream)
 
 
 def fa_bwd_noalloc(q: int, k: int, v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int,
@@ -176,6 +184,20 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
                             do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws,
                             B, H, N, d, scale, int(bool(causal)), _stream_handle(q.device)))
     return dq, dk, dv
+
+
+def backward_stage(stage: int, q, k, v, o, lse, do, dq, dk, dv, workspace, causal: bool = False,
+                   scale: float | None = None):
+    """One backward stage through fa_bwd_stage on the current stream."""
+    import torch
+    _check_inputs(q, k, v, do)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    _check(f"fa_bwd_stage({stage})",
+           fa_bwd_stage(stage, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                        B, H, N, d, scale, int(bool(causal)), _stream_handle(q.device)))
 
 
 def sync_status(device=None) -> None:

@@ -268,6 +268,49 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const floa
   return fa::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const float* o, const float* lse,
+                       const void* dO, float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d,
+                       float scale, int causal, fa_stream_t stream) {
+  if (stage < 0 || stage > 2) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, N, d, causal);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, 4))
+    return FA_ERR_MISALIGNED;
+  DeviceInfo di;
+  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
+  const int heads = B * H;
+  fa::BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_bf16_map(&a.tm_q, q, heads, N, d) || !encode_bf16_map(&a.tm_k, k, heads, N, d) ||
+      !encode_bf16_map(&a.tm_v, v, heads, N, d) || !encode_bf16_map(&a.tm_do, dO, heads, N, d))
+    return FA_ERR_LAUNCH;
+  a.o = o;
+  a.lse = lse;
+  a.dout = static_cast<const uint16_t*>(dO);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.delta = workspace;
+  a.heads = heads;
+  a.n = N;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.sched_kv = make_sched(heads, N, d, causal, di.sms, 0, fa::kTileRows, 0);
+  a.sched_q = make_sched(heads, N, d, causal, di.sms, 0, fa::kTileRows, 1);
+  a.grid_kv = a.sched_kv.grid;
+  a.grid_q = a.sched_q.grid;
+  a.grid_pre = 2 * di.sms;
+  a.status = di.status;
+  a.wait_limit_ns = wait_limit_ns();
+  return fa::launch_bwd_stage(a, stage, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                              : FA_ERR_LAUNCH;
+}
+
 fa_status fa_sync_status(fa_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_DEVICE_FAULT;
   int h[4] = {0, 0, 0, 0};

@@ -794,12 +794,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
-  const int rows = a.heads * a.n;
-  preprocess_kernel<D><<<a.grid_pre, 256, 0, stream>>>(a.o, a.dout, a.delta, rows);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  {
+cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
+  cudaError_t e = cudaSuccess;
+  if (stage == 0) {
+    preprocess_kernel<D><<<a.grid_pre, 256, 0, stream>>>(a.o, a.dout, a.delta, a.heads * a.n);
+  } else if (stage == 1) {
     // dQ first: it turns D' = rowsum(dO o O) into the exact row term
     using L = QLayout<D>;
     auto kern = dq_kernel<D, CAUSAL>;
@@ -808,10 +807,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     kern<<<a.grid_q, kQThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dq,
                                                          a.n, a.scale, a.scale_log2, a.sched_q, a.status,
                                                          a.wait_limit_ns);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  {
+  } else {
     using L = KvLayout<D>;
     auto kern = dkdv_kernel<D, CAUSAL>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
@@ -819,9 +815,17 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     kern<<<a.grid_kv, kKvThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dk,
                                                            a.dv, a.n, a.scale, a.scale_log2, a.sched_kv, a.status,
                                                            a.wait_limit_ns);
-    e = cudaGetLastError();
   }
-  return e;
+  return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+  for (int stage = 0; stage < 3; ++stage) {
+    const cudaError_t e = launch_stage_t<D, CAUSAL>(a, stage, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -829,6 +833,12 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
   if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
   return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+}
+
+cudaError_t launch_bwd_stage(const BwdArgs& a, int stage, cudaStream_t stream) {
+  if (a.d == 64)
+    return a.causal ? launch_stage_t<64, true>(a, stage, stream) : launch_stage_t<64, false>(a, stage, stream);
+  return a.causal ? launch_stage_t<128, true>(a, stage, stream) : launch_stage_t<128, false>(a, stage, stream);
 }
 
 }  // namespace fa

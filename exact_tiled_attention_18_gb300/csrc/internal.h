@@ -51,4 +51,8 @@ struct BwdArgs {
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 
+// The three stages of launch_bwd, for callers that time or order them
+// separately: 0 = preprocess (D'), 1 = dQ (corrects D), 2 = dK/dV.
+cudaError_t launch_bwd_stage(const BwdArgs& a, int stage, cudaStream_t stream);
+
 }  // namespace fa

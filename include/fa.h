@@ -132,6 +132,20 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const floa
                          const void* dO, float* dq, float* dk, float* dv, int B, int H, int N, int d, float scale,
                          int causal, fa_stream_t stream);
 
+/*
+ * One stage of fa_bwd, for callers that time or schedule the three kernels
+ * separately; running stages 0, 1, 2 in order on one stream is exactly
+ * fa_bwd with a caller-owned workspace (here required, never NULL).
+ *   stage 0: D'_i = sum_c dO_ic O_ic into the workspace (reads o, dO only).
+ *   stage 1: dQ; also rewrites the workspace with the exact row term
+ *            D_i = sum_j P_ij dP_ij (needs stage 0 first).
+ *   stage 2: dK and dV (needs stage 1 first).
+ * Arguments as fa_bwd; a stage outside 0..2 returns FA_ERR_INVALID_ARG.
+ */
+fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const float* o, const float* lse,
+                       const void* dO, float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d,
+                       float scale, int causal, fa_stream_t stream);
+
 /* Bytes of the fa_bwd workspace: B*H*N fp32 values (0 on invalid sizes). */
 size_t fa_bwd_workspace_bytes(int B, int H, int N);
 

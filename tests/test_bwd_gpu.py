@@ -102,3 +102,19 @@ def test_backward_full_size_whole_heads(name, heads):
         rq, rk, rv, _ = oracle.backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal)
         got = tuple(t[b:b + 1, h:h + 1] for t in (dq, dk, dv))
         check_grads(got, (rq, rk, rv), f"{name} head {(b, h)}")
+
+
+def test_stages_equal_fa_bwd():
+    """fa_bwd_stage 0, 1, 2 in order is exactly fa_bwd."""
+    inp = workloads.make_inputs(2, 2, 300, 128, seed=31, with_grad=True)
+    scale = scale_for(128)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=True, scale=scale)
+    ref = fa.backward(q, k, v, o, lse, do, causal=True, scale=scale)
+    ws = torch.empty(2 * 2 * 300, dtype=torch.float32, device="cuda")
+    out = [torch.empty_like(x) for x in ref]
+    for stage in range(3):
+        fa.backward_stage(stage, q, k, v, o, lse, do, *out, ws, causal=True, scale=scale)
+    fa.sync_status()
+    for a, b in zip(out, ref):
+        assert torch.equal(a, b)
