@@ -22,6 +22,7 @@
 //   warps 4-7  softmax for tile B
 //   warp  8    TMA producer (one thread)
 //   warp  9    tcgen05 MMA issuer (one thread); owns the TMEM allocation
+//   warps 10-11 idle (complete the third warpgroup for the register split)
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128) S_A, [128,256) S_B, [256,256+d) O_A, [256+d,256+2d) O_B.
 //   P (bf16, two per column) overwrites the first 64 columns of its S region
@@ -37,7 +38,17 @@
 namespace fa {
 namespace {
 
-constexpr int kFwdThreads = 320;
+// 12 warps: two softmax warpgroups, then TMA (warp 8), MMA (warp 9) and two
+// idle warps that only complete the third warpgroup.  Launched at 168
+// registers a thread (384 x 168 = 64512); the softmax warpgroups then take 192
+// (no spills) and the third warpgroup keeps 120, enough for the MMA thread:
+// 2*128*192 + 128*120 = 64512.
+constexpr int kFwdThreads = 384;
+constexpr int kFwdLaunchRegs = 168;
+constexpr int kFwdSoftmaxRegs = 192;
+constexpr int kFwdOtherRegs = 120;
+static_assert(2 * 128 * kFwdSoftmaxRegs + 128 * kFwdOtherRegs <= kFwdThreads * kFwdLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr float kTau = 8.0f;  // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -153,6 +164,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (warp < 8) {
     // ------------------------------------------------------------ softmax
+    regs_increase<kFwdSoftmaxRegs>();
     const int t = warp >> 2;
     const int r = ((warp & 3) << 5) + lane;  // row inside the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
@@ -189,15 +201,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -CUDART_INF_F;
         }
-        float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, m2 = -CUDART_INF_F, m3 = -CUDART_INF_F;
+        // row maximum as a log-depth tree of 3-input max
+        float t1[43];
 #pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-          m0 = fmax3(m0, s[c + 0], s[c + 1]);
-          m1 = fmax3(m1, s[c + 2], s[c + 3]);
-          m2 = fmax3(m2, s[c + 4], s[c + 5]);
-          m3 = fmax3(m3, s[c + 6], s[c + 7]);
-        }
-        const float mt = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * scale_log2;
+        for (int c = 0; c < 42; ++c) t1[c] = fmax3(s[3 * c], s[3 * c + 1], s[3 * c + 2]);
+        t1[42] = fmaxf(s[126], s[127]);
+        float t2[15];
+#pragma unroll
+        for (int c = 0; c < 14; ++c) t2[c] = fmax3(t1[3 * c], t1[3 * c + 1], t1[3 * c + 2]);
+        t2[14] = t1[42];
+        float t3[5];
+#pragma unroll
+        for (int c = 0; c < 5; ++c) t3[c] = fmax3(t2[3 * c], t2[3 * c + 1], t2[3 * c + 2]);
+        const float mt = fmaxf(fmax3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4])) * scale_log2;
         if (j == 0) {
           m_ref = (mt == -CUDART_INF_F) ? 0.f : mt;
         } else {
@@ -221,27 +237,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_st_wait();
           }
         }
-        const float neg = -m_ref;
-        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+        // P = 2^(s*c - m_ref) in bf16 over the first 64 S columns; two lanes
+        // of the scale-subtract and of the running sum per instruction
+        const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+        const uint64_t n2 = f2_pack(-m_ref, -m_ref);
+        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
-            const float p0 = ex2_approx(fmaf(s[32 * c + 2 * i + 0], scale_log2, neg));
-            const float p1 = ex2_approx(fmaf(s[32 * c + 2 * i + 1], scale_log2, neg));
-            const float p2 = ex2_approx(fmaf(s[32 * c + 2 * i + 2], scale_log2, neg));
-            const float p3 = ex2_approx(fmaf(s[32 * c + 2 * i + 3], scale_log2, neg));
-            l0 += p0;
-            l1 += p1;
-            l2 += p2;
-            l3 += p3;
+            float x0, x1, x2, x3;
+            f2_unpack(ffma2(f2_pack(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), c2, n2), x0, x1);
+            f2_unpack(ffma2(f2_pack(s[32 * c + 2 * i + 2], s[32 * c + 2 * i + 3]), c2, n2), x2, x3);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            acc0 = fadd2(acc0, f2_pack(p0, p1));
+            acc1 = fadd2(acc1, f2_pack(p2, p3));
             pk[i] = pack_bf16x2(p0, p1);
             pk[i + 1] = pack_bf16x2(p2, p3);
           }
           tmem_st16(tS + 16 * c, pk);
         }
-        l += (l0 + l1) + (l2 + l3);
+        float a0, a1, a2, a3;
+        f2_unpack(acc0, a0, a1);
+        f2_unpack(acc1, a2, a3);
+        l += (a0 + a1) + (a2 + a3);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(L::P_FULL + t));
@@ -274,7 +294,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (valid) lse[static_cast<size_t>(head) * n + row] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -CUDART_INF_F;
     }
-  } else if (warp == 8) {
+  } else {
+   regs_decrease<kFwdOtherRegs>();
+   if (warp == 8) {
     // -------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_last();
@@ -324,7 +346,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
@@ -409,6 +431,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       umma_commit(BAR(L::DRAIN));
       drain_wait(BAR(L::DRAIN), 0, limit_ns);
     }
+   }
   }
 
   tc_fence_before();
@@ -424,7 +447,12 @@ template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
   auto kern = fwd_kernel<D, CAUSAL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  cudaFuncAttributes fattr;
+  cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
+  if (e != cudaSuccess) return e;
+  // the warpgroup register split assumes this launch allocation
+  if (fattr.numRegs != kFwdLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<a.sched.grid, kFwdThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.n,
                                                              a.scale_log2, a.sched, a.status, a.wait_limit_ns);
