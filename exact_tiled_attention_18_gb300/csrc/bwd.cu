@@ -74,10 +74,16 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_
 // every 64th query by 10) amplify a plain bf16 rounding of dS past the
 // gradient tolerance.
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const uint32_t b0 = __float_as_uint(x0) & 0xFFFF0000u;
-  const uint32_t b1 = __float_as_uint(x1) & 0xFFFF0000u;
-  hi = __byte_perm(b0, b1, 0x7632);
-  lo = pack_bf16x2(x0 - __uint_as_float(b0), x1 - __uint_as_float(b1));
+  const uint32_t u0 = __float_as_uint(x0), u1 = __float_as_uint(x1);
+  hi = __byte_perm(u0, u1, 0x7632);  // top halves of both: truncation to bf16
+  float r0, r1;
+  f2_unpack(fsub2(f2_pack(x0, x1), f2_pack(__uint_as_float(u0 & 0xFFFF0000u), __uint_as_float(u1 & 0xFFFF0000u))),
+            r0, r1);
+  lo = pack_bf16x2(r0, r1);
+}
+
+__device__ __forceinline__ uint64_t f2_from(uint32_t a, uint32_t b) {
+  return f2_pack(__uint_as_float(a), __uint_as_float(b));
 }
 
 // ------------------------------------------------------------------ preprocess
@@ -140,7 +146,16 @@ struct KvLayout {
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
 };
 
-constexpr int kKvThreads = 352;  // 8 elementwise warps, TMA, MMA, LSE/D loader
+// 12 warps: two elementwise warpgroups, then TMA (warp 8), MMA (warp 9), the
+// LSE/D loader (warp 10) and an idle warp completing the third warpgroup.
+// Launched at 168 registers a thread; the elementwise warpgroups take 192 and
+// the third keeps 120 (2*128*192 + 128*120 = 384*168).
+constexpr int kKvThreads = 384;
+constexpr int kKvLaunchRegs = 168;
+constexpr int kKvEwRegs = 192;
+constexpr int kKvOtherRegs = 120;
+static_assert(2 * 128 * kKvEwRegs + 128 * kKvOtherRegs <= kKvThreads * kKvLaunchRegs,
+              "register split exceeds the launch allocation");
 
 // Query tiles that see key tile j.
 __device__ __forceinline__ void kv_range(int j, int nt, bool causal, int& i0, int& i1) {
@@ -202,6 +217,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
   if (warp < 8) {
     // ------------------------------------------------ P^T and dS^T (thread = key row)
+    regs_increase<kKvEwRegs>();
     const int w = warp >> 2;  // warpgroup: query columns [64 w, 64 w + 64)
     const int r = ((warp & 3) << 5) + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
@@ -225,24 +241,28 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const float* l2s = ld_base + ls * 256;
         const float* dds = l2s + 128;
         const bool diag = CAUSAL && (i == j);
+        const uint64_t c2 = f2_pack(scale_log2, scale_log2);
         // P^T and dS^T for 32 query columns starting at col0; P packed into pk,
         // dS split into hk (hi) and lk (lo)
         auto chunk = [&](const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&pk)[16],
                          uint32_t (&hk)[16], uint32_t (&lk)[16]) {
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
+            // l2s holds -LSE*log2(e) (-inf past the sequence end), dds holds D
             const float4 l4 = *reinterpret_cast<const float4*>(l2s + col0 + c);
             const float4 d4 = *reinterpret_cast<const float4*>(dds + col0 + c);
-            const float la[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float da[4] = {d4.x, d4.y, d4.z, d4.w};
             float p[4], ds[4];
+            f2_unpack(ffma2(f2_from(sr[c], sr[c + 1]), c2, f2_pack(l4.x, l4.y)), p[0], p[1]);
+            f2_unpack(ffma2(f2_from(sr[c + 2], sr[c + 3]), c2, f2_pack(l4.z, l4.w)), p[2], p[3]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              float pe = ex2_approx(fmaf(__uint_as_float(sr[c + e]), scale_log2, -la[e]));
-              if (diag && (col0 + c + e) < r) pe = 0.f;  // query before key: masked
-              p[e] = pe;
-              ds[e] = pe * (__uint_as_float(dr[c + e]) - da[e]);
+              p[e] = ex2_approx(p[e]);
+              if (diag && (col0 + c + e) < r) p[e] = 0.f;  // query before key: masked
             }
+            f2_unpack(fmul2(f2_pack(p[0], p[1]), fsub2(f2_from(dr[c], dr[c + 1]), f2_pack(d4.x, d4.y))), ds[0],
+                      ds[1]);
+            f2_unpack(fmul2(f2_pack(p[2], p[3]), fsub2(f2_from(dr[c + 2], dr[c + 3]), f2_pack(d4.z, d4.w))), ds[2],
+                      ds[3]);
             pk[c / 2] = pack_bf16x2(p[0], p[1]);
             pk[c / 2 + 1] = pack_bf16x2(p[2], p[3]);
             split_bf16x2(ds[0], ds[1], hk[c / 2], lk[c / 2]);
@@ -308,7 +328,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
       }
     }
-  } else if (warp == 8) {
+  } else {
+   regs_decrease<kKvOtherRegs>();
+   if (warp == 8) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol_keep = l2_policy_evict_last();
@@ -430,7 +452,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       umma_commit(BAR(L::DRAIN));
       drain_wait(BAR(L::DRAIN), 0, limit_ns);
     }
-  } else {
+  } else if (warp == 10) {
     // ------------------------------------------- LSE / D rows of each query tile
     const float* lse_h = nullptr;
     uint32_t ldn = 0;
@@ -454,13 +476,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           const int idx = lane * 4 + t;
           const int q = i * kTileRows + idx;
           const bool in = q < n;
-          l2s[idx] = in ? lse_h[q] * kLog2e : CUDART_INF_F;
+          l2s[idx] = in ? -lse_h[q] * kLog2e : -CUDART_INF_F;
           l2s[128 + idx] = in ? d_h[q] : 0.f;
         }
         mbar_arrive(BAR(L::LD_FULL + ls));
         ++ldn;
       }
     }
+  }
   }
 
   tc_fence_before();
@@ -578,6 +601,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const float l2 = valid ? lse[static_cast<size_t>(head) * n + row] * kLog2e : CUDART_INF_F;
       const float dd = valid ? delta[static_cast<size_t>(head) * n + row] : 0.f;
       const float nl2 = -l2;
+      const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+      const uint64_t nl2x2 = f2_pack(nl2, nl2);
+      const uint64_t dd2 = f2_pack(dd, dd);
       float dsum = 0.f;  // this warpgroup's share of delta_i
       for (int jt = 0; jt < nk; ++jt) {
         ok = warp_wait(BAR(L::SDP_FULL), sn & 1, wc, SITE_Q_EW_SDP, unit);
@@ -590,21 +616,24 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const int lim = (diag || tail) ? ((CAUSAL ? min(row + 1, n) : n) - jt * kTileRows) : kTileRows;
         auto chunk = [&](const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&pk)[16],
                          uint32_t (&hk)[16], uint32_t (&lk)[16]) {
-          float acc0 = 0.f, acc1 = 0.f;
+          uint64_t acc = f2_pack(0.f, 0.f);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), scale_log2, nl2));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), scale_log2, nl2));
+            float p0, p1, ds0, ds1;
+            f2_unpack(ffma2(f2_from(sr[c], sr[c + 1]), c2, nl2x2), p0, p1);
+            p0 = ex2_approx(p0);
+            p1 = ex2_approx(p1);
             if (col0 + c >= lim) p0 = 0.f;
             if (col0 + c + 1 >= lim) p1 = 0.f;
-            const float ds0 = p0 * (__uint_as_float(dr[c]) - dd);
-            const float ds1 = p1 * (__uint_as_float(dr[c + 1]) - dd);
-            acc0 += ds0;
-            acc1 += ds1;
+            const uint64_t ds01 = fmul2(f2_pack(p0, p1), fsub2(f2_from(dr[c], dr[c + 1]), dd2));
+            acc = fadd2(acc, ds01);
+            f2_unpack(ds01, ds0, ds1);
             pk[c / 2] = pack_bf16x2(p0, p1);
             split_bf16x2(ds0, ds1, hk[c / 2], lk[c / 2]);
           }
-          dsum += acc0 + acc1;
+          float a0, a1;
+          f2_unpack(acc, a0, a1);
+          dsum += a0 + a1;
         };
         // Each store lands on columns this thread has already read.
         const uint32_t tS = tmem + lane_off + L::kColS + 64 * w;
@@ -810,6 +839,11 @@ cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
   } else {
     using L = KvLayout<D>;
     auto kern = dkdv_kernel<D, CAUSAL>;
+    cudaFuncAttributes fattr;
+    e = cudaFuncGetAttributes(&fattr, kern);
+    if (e != cudaSuccess) return e;
+    // the warpgroup register split assumes this launch allocation
+    if (fattr.numRegs != kKvLaunchRegs) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<a.grid_kv, kKvThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dk,
