@@ -25,6 +25,8 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -187,11 +189,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(bars + 8 * (L::QD_FULL + s), 1);
       mbar_init(bars + 8 * (L::QD_EMPTY + s), 1);
-      mbar_init(bars + 8 * (L::LD_FULL + s), 32);
-      mbar_init(bars + 8 * (L::LD_EMPTY + s), 256);
+      mbar_init(bars + 8 * (L::LD_FULL + s), 1);    // the loader warp
+      mbar_init(bars + 8 * (L::LD_EMPTY + s), 8);   // one per elementwise warp
     }
     mbar_init(bars + 8 * L::SDP_FULL, 1);
-    mbar_init(bars + 8 * L::PDS_FULL, 256);
+    mbar_init(bars + 8 * L::PDS_FULL, 8);
     mbar_init(bars + 8 * L::ACC_FULL, 1);
     mbar_init(bars + 8 * L::DRAIN, 1);
     *abort_flag = 0;
@@ -241,10 +243,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const float* l2s = ld_base + ls * 256;
         const float* dds = l2s + 128;
         const bool diag = CAUSAL && (i == j);
+        const bool need_mask = diag;
         const uint64_t c2 = f2_pack(scale_log2, scale_log2);
         // P^T and dS^T for 32 query columns starting at col0; P packed into pk,
         // dS split into hk (hi) and lk (lo)
-        auto chunk = [&](const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&pk)[16],
+        // MASKED: diagonal tile, where a key may come after the query
+        auto chunk = [&](auto masked, const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&pk)[16],
                          uint32_t (&hk)[16], uint32_t (&lk)[16]) {
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
@@ -257,7 +261,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               p[e] = ex2_approx(p[e]);
-              if (diag && (col0 + c + e) < r) p[e] = 0.f;  // query before key: masked
+              if (decltype(masked)::value && (col0 + c + e) < r) p[e] = 0.f;  // query before key: masked
             }
             f2_unpack(fmul2(f2_pack(p[0], p[1]), fsub2(f2_from(dr[c], dr[c + 1]), f2_pack(d4.x, d4.y))), ds[0],
                       ds[1]);
@@ -276,27 +280,30 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const uint32_t tS = tmem + lane_off + L::kColS + 64 * w;
         const uint32_t tD = tmem + lane_off + L::kColDP + 64 * w;
         {
-          uint32_t s0[32], s1[32], d0[32], pk[16], hk[16], lk[16];
+          uint32_t s0[32], s1[32], d0[32], d1[32], pk[16], hk[16], lk[16];
           tmem_ld32(tS, s0);
           tmem_ld32(tS + 32, s1);
           tmem_ld32(tD, d0);
+          tmem_ld32(tD + 32, d1);
           tmem_ld_wait();
-          chunk(s0, d0, 64 * w, pk, hk, lk);
+          if (need_mask) chunk(std::true_type{}, s0, d0, 64 * w, pk, hk, lk);
+          else chunk(std::false_type{}, s0, d0, 64 * w, pk, hk, lk);
           tmem_st16(tS, pk);
           tmem_st16(tD, hk);
           tmem_st16(tS + 32, lk);
-          uint32_t d1[32];
-          tmem_ld32(tD + 32, d1);
-          tmem_ld_wait();
-          chunk(s1, d1, 64 * w + 32, pk, hk, lk);
+          if (need_mask) chunk(std::true_type{}, s1, d1, 64 * w + 32, pk, hk, lk);
+          else chunk(std::false_type{}, s1, d1, 64 * w + 32, pk, hk, lk);
           tmem_st16(tS + 16, pk);
           tmem_st16(tD + 16, hk);
           tmem_st16(tS + 48, lk);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(BAR(L::PDS_FULL));
-        mbar_arrive(BAR(L::LD_EMPTY + ls));
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(BAR(L::PDS_FULL));
+          mbar_arrive(BAR(L::LD_EMPTY + ls));
+        }
         ++ldn;
       }
       if (!ok) break;
@@ -479,7 +486,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           l2s[idx] = in ? -lse_h[q] * kLog2e : -CUDART_INF_F;
           l2s[128 + idx] = in ? d_h[q] : 0.f;
         }
-        mbar_arrive(BAR(L::LD_FULL + ls));
+        mbar_arrive_warp(BAR(L::LD_FULL + ls));
         ++ldn;
       }
     }
@@ -524,7 +531,9 @@ struct QLayout {
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColB = 256 + D;
 };
 
-constexpr int kQThreads = 320;  // 8 elementwise warps, TMA, MMA
+// 12 warps: two elementwise warpgroups, TMA (warp 8), MMA (warp 9) and two idle
+// warps completing the third warpgroup; same register split as dK/dV.
+constexpr int kQThreads = 384;
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kQThreads, 1)
@@ -552,9 +561,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
       mbar_init(bars + 8 * (L::KV_EMPTY + s), 1);
     }
     mbar_init(bars + 8 * L::SDP_FULL, 1);
-    mbar_init(bars + 8 * L::DS_FULL, 256);
+    mbar_init(bars + 8 * L::DS_FULL, 8);
     mbar_init(bars + 8 * L::ACC_FULL, 1);
-    mbar_init(bars + 8 * L::XCH, 256);
+    mbar_init(bars + 8 * L::XCH, 8);
     mbar_init(bars + 8 * L::DRAIN, 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -579,6 +588,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
   if (warp < 8) {
     // ------------------------------------------------- dS (thread = query row)
+    regs_increase<kKvEwRegs>();
     // The row term comes in as D'_i = rowsum(dO o O) with O from the forward
     // pass, whose P was rounded to bf16 for the PV product.  The kernel sees
     // every key of its rows, so it also sums delta_i = sum_j dS'_ij =
@@ -613,8 +623,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const bool diag = CAUSAL && (jt == i);
         const bool tail = (jt == nt - 1) && ((n & (kTileRows - 1)) != 0);
         // number of eligible key columns of this tile for this row
-        const int lim = (diag || tail) ? ((CAUSAL ? min(row + 1, n) : n) - jt * kTileRows) : kTileRows;
-        auto chunk = [&](const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&pk)[16],
+        const bool need_mask = diag || tail;
+        const int lim = need_mask ? ((CAUSAL ? min(row + 1, n) : n) - jt * kTileRows) : kTileRows;
+        // MASKED: diagonal or tail tile, where some key columns are not eligible
+        auto chunk = [&](auto masked, const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&pk)[16],
                          uint32_t (&hk)[16], uint32_t (&lk)[16]) {
           uint64_t acc = f2_pack(0.f, 0.f);
 #pragma unroll
@@ -623,8 +635,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
             f2_unpack(ffma2(f2_from(sr[c], sr[c + 1]), c2, nl2x2), p0, p1);
             p0 = ex2_approx(p0);
             p1 = ex2_approx(p1);
-            if (col0 + c >= lim) p0 = 0.f;
-            if (col0 + c + 1 >= lim) p1 = 0.f;
+            if (decltype(masked)::value) {
+              if (col0 + c >= lim) p0 = 0.f;
+              if (col0 + c + 1 >= lim) p1 = 0.f;
+            }
             const uint64_t ds01 = fmul2(f2_pack(p0, p1), fsub2(f2_from(dr[c], dr[c + 1]), dd2));
             acc = fadd2(acc, ds01);
             f2_unpack(ds01, ds0, ds1);
@@ -639,32 +653,32 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const uint32_t tS = tmem + lane_off + L::kColS + 64 * w;
         const uint32_t tD = tmem + lane_off + L::kColDP + 64 * w;
         {
-          uint32_t s0[32], s1[32], d0[32], pk[16], hk[16], lk[16];
+          uint32_t s0[32], s1[32], d0[32], d1[32], pk[16], hk[16], lk[16];
           tmem_ld32(tS, s0);
           tmem_ld32(tS + 32, s1);
           tmem_ld32(tD, d0);
+          tmem_ld32(tD + 32, d1);
           tmem_ld_wait();
-          chunk(s0, d0, 64 * w, pk, hk, lk);
+          if (need_mask) chunk(std::true_type{}, s0, d0, 64 * w, pk, hk, lk);
+          else chunk(std::false_type{}, s0, d0, 64 * w, pk, hk, lk);
           tmem_st16(tS, pk);
           tmem_st16(tD, hk);
           tmem_st16(tS + 32, lk);
-          uint32_t d1[32];
-          tmem_ld32(tD + 32, d1);
-          tmem_ld_wait();
-          chunk(s1, d1, 64 * w + 32, pk, hk, lk);
+          if (need_mask) chunk(std::true_type{}, s1, d1, 64 * w + 32, pk, hk, lk);
+          else chunk(std::false_type{}, s1, d1, 64 * w + 32, pk, hk, lk);
           tmem_st16(tS + 16, pk);
           tmem_st16(tD + 16, hk);
           tmem_st16(tS + 48, lk);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(BAR(L::DS_FULL));
+        mbar_arrive_warp(BAR(L::DS_FULL));
       }
       if (!ok) break;
       // combine the two warpgroups' halves of delta_i (slots alternate by unit)
       float* slot = xch + (an & 1) * 256;
       slot[w * 128 + r] = dsum;
-      mbar_arrive(BAR(L::XCH));
+      mbar_arrive_warp(BAR(L::XCH));
       ok = warp_wait(BAR(L::XCH), an & 1, wc, SITE_Q_EW_XCH, unit);
       if (!ok) break;
       const float dlt = slot[r] + slot[128 + r];
@@ -694,7 +708,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
       }
     }
-  } else if (warp == 8) {
+  } else {
+   regs_decrease<kKvOtherRegs>();
+   if (warp == 8) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol_keep = l2_policy_evict_last();
@@ -742,7 +758,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
@@ -813,6 +829,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
   }
 
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 9) {
@@ -831,6 +848,10 @@ cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
     // dQ first: it turns D' = rowsum(dO o O) into the exact row term
     using L = QLayout<D>;
     auto kern = dq_kernel<D, CAUSAL>;
+    cudaFuncAttributes fattr;
+    e = cudaFuncGetAttributes(&fattr, kern);
+    if (e != cudaSuccess) return e;
+    if (fattr.numRegs != kKvLaunchRegs) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<a.grid_q, kQThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dq,

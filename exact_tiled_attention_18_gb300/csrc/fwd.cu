@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bars + 8 * (L::S_FULL + t), 1);
-      mbar_init(bars + 8 * (L::P_FULL + t), 128);
+      mbar_init(bars + 8 * (L::P_FULL + t), 4);  // one arrive per softmax warp
       mbar_init(bars + 8 * (L::O_FULL + t), 1);
     }
     mbar_init(bars + 8 * L::DRAIN, 1);
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         l += (a0 + a1) + (a2 + a3);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(BAR(L::P_FULL + t));
+        mbar_arrive_warp(BAR(L::P_FULL + t));
       }
       if (!ok) break;
       // epilogue: O = accumulator / l, LSE = ln(sum exp(scaled scores))
