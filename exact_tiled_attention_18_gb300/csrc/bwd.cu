@@ -138,8 +138,9 @@ struct KvLayout {
   static constexpr int LD_FULL = QD_EMPTY + kStages;
   static constexpr int LD_EMPTY = LD_FULL + kStages;
   static constexpr int SDP_FULL = LD_EMPTY + kStages;
-  static constexpr int PDS_FULL = SDP_FULL + 1;
-  static constexpr int ACC_FULL = PDS_FULL + 1;
+  static constexpr int P_READY = SDP_FULL + 1;   // P^T stored (one arrive per elementwise warp)
+  static constexpr int DS_READY = P_READY + 1;   // dS^T hi/lo stored
+  static constexpr int ACC_FULL = DS_READY + 1;
   static constexpr int DRAIN = ACC_FULL + 1;
   static constexpr int kNumBars = DRAIN + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -193,7 +194,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       mbar_init(bars + 8 * (L::LD_EMPTY + s), 8);   // one per elementwise warp
     }
     mbar_init(bars + 8 * L::SDP_FULL, 1);
-    mbar_init(bars + 8 * L::PDS_FULL, 8);
+    mbar_init(bars + 8 * L::P_READY, 8);
+    mbar_init(bars + 8 * L::DS_READY, 8);
     mbar_init(bars + 8 * L::ACC_FULL, 1);
     mbar_init(bars + 8 * L::DRAIN, 1);
     *abort_flag = 0;
@@ -245,30 +247,38 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const bool diag = CAUSAL && (i == j);
         const bool need_mask = diag;
         const uint64_t c2 = f2_pack(scale_log2, scale_log2);
-        // P^T and dS^T for 32 query columns starting at col0; P packed into pk,
-        // dS split into hk (hi) and lk (lo)
-        // MASKED: diagonal tile, where a key may come after the query
-        auto chunk = [&](auto masked, const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&pk)[16],
-                         uint32_t (&hk)[16], uint32_t (&lk)[16]) {
+        // Phase 1: P^T for 32 query columns starting at col0, kept in sr as fp32
+        // bits and packed to bf16 in pk.  MASKED: diagonal tile, where a key
+        // may come after the query.
+        auto pchunk = [&](auto masked, uint32_t (&sr)[32], int col0, uint32_t (&pk)[16]) {
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
-            // l2s holds -LSE*log2(e) (-inf past the sequence end), dds holds D
+            // l2s holds -LSE*log2(e) (-inf past the sequence end)
             const float4 l4 = *reinterpret_cast<const float4*>(l2s + col0 + c);
-            const float4 d4 = *reinterpret_cast<const float4*>(dds + col0 + c);
-            float p[4], ds[4];
+            float p[4];
             f2_unpack(ffma2(f2_from(sr[c], sr[c + 1]), c2, f2_pack(l4.x, l4.y)), p[0], p[1]);
             f2_unpack(ffma2(f2_from(sr[c + 2], sr[c + 3]), c2, f2_pack(l4.z, l4.w)), p[2], p[3]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               p[e] = ex2_approx(p[e]);
               if (decltype(masked)::value && (col0 + c + e) < r) p[e] = 0.f;  // query before key: masked
+              sr[c + e] = __float_as_uint(p[e]);
             }
-            f2_unpack(fmul2(f2_pack(p[0], p[1]), fsub2(f2_from(dr[c], dr[c + 1]), f2_pack(d4.x, d4.y))), ds[0],
-                      ds[1]);
-            f2_unpack(fmul2(f2_pack(p[2], p[3]), fsub2(f2_from(dr[c + 2], dr[c + 3]), f2_pack(d4.z, d4.w))), ds[2],
-                      ds[3]);
             pk[c / 2] = pack_bf16x2(p[0], p[1]);
             pk[c / 2 + 1] = pack_bf16x2(p[2], p[3]);
+          }
+        };
+        // Phase 2: dS^T = P^T o (dP^T - D), split into hk (hi) and lk (lo)
+        auto dchunk = [&](const uint32_t (&pr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&hk)[16],
+                          uint32_t (&lk)[16]) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dds + col0 + c);
+            float ds[4];
+            f2_unpack(fmul2(f2_from(pr[c], pr[c + 1]), fsub2(f2_from(dr[c], dr[c + 1]), f2_pack(d4.x, d4.y))), ds[0],
+                      ds[1]);
+            f2_unpack(fmul2(f2_from(pr[c + 2], pr[c + 3]), fsub2(f2_from(dr[c + 2], dr[c + 3]), f2_pack(d4.z, d4.w))),
+                      ds[2], ds[3]);
             split_bf16x2(ds[0], ds[1], hk[c / 2], lk[c / 2]);
             split_bf16x2(ds[2], ds[3], hk[c / 2 + 1], lk[c / 2 + 1]);
           }
@@ -276,24 +286,32 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         // Column slice of this warpgroup: S^T [64w, 64w+64), dP^T likewise.
         // After use the slice holds P^T in S cols [64w, 64w+32), dS^T lo in
         // S cols [64w+32, 64w+64) and dS^T hi in dP cols [64w, 64w+32); every
-        // store lands on columns this thread has already read.
+        // store lands on columns this thread has already read.  P^T is
+        // published first so the MMA thread can run dV += P^T dO while dS^T is
+        // still being computed.
         const uint32_t tS = tmem + lane_off + L::kColS + 64 * w;
         const uint32_t tD = tmem + lane_off + L::kColDP + 64 * w;
         {
           uint32_t s0[32], s1[32], d0[32], d1[32], pk[16], hk[16], lk[16];
           tmem_ld32(tS, s0);
           tmem_ld32(tS + 32, s1);
-          tmem_ld32(tD, d0);
-          tmem_ld32(tD + 32, d1);
           tmem_ld_wait();
-          if (need_mask) chunk(std::true_type{}, s0, d0, 64 * w, pk, hk, lk);
-          else chunk(std::false_type{}, s0, d0, 64 * w, pk, hk, lk);
+          if (need_mask) pchunk(std::true_type{}, s0, 64 * w, pk);
+          else pchunk(std::false_type{}, s0, 64 * w, pk);
           tmem_st16(tS, pk);
+          if (need_mask) pchunk(std::true_type{}, s1, 64 * w + 32, pk);
+          else pchunk(std::false_type{}, s1, 64 * w + 32, pk);
+          tmem_st16(tS + 16, pk);
+          tmem_ld32(tD, d0);  // dP arrives while P is being published
+          tmem_ld32(tD + 32, d1);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive_warp(BAR(L::P_READY));
+          tmem_ld_wait();
+          dchunk(s0, d0, 64 * w, hk, lk);
           tmem_st16(tD, hk);
           tmem_st16(tS + 32, lk);
-          if (need_mask) chunk(std::true_type{}, s1, d1, 64 * w + 32, pk, hk, lk);
-          else chunk(std::false_type{}, s1, d1, 64 * w + 32, pk, hk, lk);
-          tmem_st16(tS + 16, pk);
+          dchunk(s1, d1, 64 * w + 32, hk, lk);
           tmem_st16(tD + 16, hk);
           tmem_st16(tS + 48, lk);
         }
@@ -301,7 +319,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(BAR(L::PDS_FULL));
+          mbar_arrive(BAR(L::DS_READY));
           mbar_arrive(BAR(L::LD_EMPTY + ls));
         }
         ++ldn;
@@ -423,13 +441,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     sdesc_sw128(da + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::SDP_FULL));
-          ok = wait_bounded(BAR(L::PDS_FULL), pn & 1, wc, SITE_KV_MMA_PDS, unit);
-          if (!ok) break;
-          ++pn;
-          tc_fence_after();
           // dV += P^T dO and dK += dS^T Q: M = 128 keys, N = d, K = 128 queries.
           // P^T / dS^T of queries [64 w, 64 w + 64) sit in the first 32 columns of
-          // the warpgroup's 64-column slice.
+          // the warpgroup's 64-column slice.  dV only needs P^T, published first.
+          ok = wait_bounded(BAR(L::P_READY), pn & 1, wc, SITE_KV_MMA_PDS, unit);
+          if (!ok) break;
+          tc_fence_after();
           const bool first = (i == i0);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
@@ -437,6 +454,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             umma_ts(tmem + L::kColDV, tmem + L::kColS + acol, sdesc_sw128(da + ks * 2048, kTileRows * 128, 1024),
                     id_acc, (!first || ks > 0) ? 1u : 0u);
           }
+          ok = wait_bounded(BAR(L::DS_READY), pn & 1, wc, SITE_KV_MMA_PDS, unit);
+          if (!ok) break;
+          ++pn;
+          tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
