@@ -88,6 +88,15 @@ unsigned long long wait_limit_ns() {
   return v;
 }
 
+// Testing only: FA_TEST_STALL_UNIT=n makes CTA 0 of the next forward launches
+// skip one K tile of the n-th work unit it processes, so that a pipeline wait
+// runs out and the timeout path can be exercised without faulting anything.
+// Read on every call; unset (the default) means never.
+int test_stall_unit() {
+  const char* s = std::getenv("FA_TEST_STALL_UNIT");
+  return (s && *s) ? std::atoi(s) : -1;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 fa_status check_sizes(int B, int H, int N, int d, int causal) {
@@ -140,6 +149,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, float* o, float* l
   a.sched = make_sched(heads, N, d, causal, di.sms, 0);
   a.status = di.status;
   a.wait_limit_ns = wait_limit_ns();
+  a.stall_unit = test_stall_unit();
   return fa::launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

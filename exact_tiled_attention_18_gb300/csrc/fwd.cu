@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, float* __restrict__ o, float* __restrict__ lse,
                const int n, const float scale_log2, const SchedParams sp, int* status,
-               const unsigned long long limit_ns) {
+               const unsigned long long limit_ns, const int stall_unit) {
   using L = FwdLayout<D>;
   constexpr int S = L::kSlots;
   extern __shared__ uint8_t smem_raw[];
@@ -325,6 +325,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const uint32_t slot = kvpos % S, use = kvpos / S;
             ok = wait_bounded(BAR(L::KV_EMPTY + slot), (use & 1) ^ 1, wc, SITE_LOAD_KV, unit);
             if (!ok) break;
+            if (blockIdx.x == 0 && static_cast<int>(qn) - 1 == stall_unit && j == 0 && w == 0) {
+              // testing hook: leave this K tile unloaded so the waits on it
+              // run out and the kernel reports a timeout instead of hanging
+              ++kvpos;
+              continue;
+            }
             mbar_arrive_expect_tx(BAR(L::KV_FULL + slot), L::kTileBytes);
             const CUtensorMap* tm = (w == 0) ? &tm_k : &tm_v;
 #pragma unroll
@@ -455,7 +461,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
   kern<<<a.sched.grid, kFwdThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.n,
-                                                             a.scale_log2, a.sched, a.status, a.wait_limit_ns);
+                                                             a.scale_log2, a.sched, a.status, a.wait_limit_ns,
+                                                             a.stall_unit);
   return cudaGetLastError();
 }
 

@@ -21,6 +21,7 @@ struct FwdArgs {
   SchedParams sched;
   int* status;                   // device status word (4 ints)
   unsigned long long wait_limit_ns;
+  int stall_unit;                // testing: CTA 0 skips one K tile of its n-th unit (-1: never)
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);

@@ -38,7 +38,11 @@
  *    pipeline wait that ran past its time limit) is recorded in a status word
  *    on the device and reported by fa_sync_status().  Every wait inside the
  *    kernels is bounded (4 s by default; the FA_WAIT_LIMIT_MS environment
- *    variable changes it), so a failing kernel returns instead of hanging.
+ *    variable, read once per process, changes it), so a failing kernel
+ *    returns instead of hanging.  For tests of that path only,
+ *    FA_TEST_STALL_UNIT=n (read on every fa_fwd call) makes the first CTA
+ *    leave one K tile of its n-th work unit unloaded: its waits run out and
+ *    fa_sync_status() then reports FA_ERR_TIMEOUT.
  *  - Thread safety: calls may be made from several host threads; calls on
  *    different devices are independent.
  */
