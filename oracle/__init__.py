@@ -8,10 +8,12 @@ its Python binding) never imports it and shares no code with it.
 from .attention import (  # noqa: F401
     backward,
     backward_head,
+    backward_varlen,
     eligible,
     forward,
     forward_head,
     forward_rows,
+    forward_varlen,
     score_matrix_payload_bytes,
     scores,
     tensor_payload_bytes,

@@ -28,8 +28,14 @@ Readings where the pages are silent (each is also a test pin or an argument):
 
 * tensors are [B, H, N, d], one (b, h) pair is one head, queries and keys have
   the same length N;
-* the mask is either none or causal, where key j is eligible for query i iff
-  j <= i;
+* the mask is either none or causal; with Nq queries and Nk keys, causal key
+  j is eligible for query i iff j <= i + (Nk - Nq): the last query sits at the
+  last key ("Do not infer the correct causal mask solely from a square
+  training example" -- same page, section "Does subtracting the maximum solve
+  every numerical issue?").  For Nq == Nk this is j <= i; one query (decoding)
+  sees every key; if Nq > Nk the first Nq - Nk queries see none;
+* padded batches carry a valid length per sequence; rows past it are padding
+  and are defined as O = 0, LSE = -inf (gradients 0);
 * the log-sum-exp is in natural-log units of the scaled scores:
   LSE_i = ln sum_j exp(s_ij) over eligible j;
 * ``scale`` is an argument (the pages' 1/sqrt(d) is the caller's default);
@@ -52,8 +58,10 @@ __all__ = [
     "forward_head",
     "forward",
     "forward_rows",
+    "forward_varlen",
     "backward_head",
     "backward",
+    "backward_varlen",
     "score_matrix_payload_bytes",
     "tensor_payload_bytes",
 ]
@@ -67,14 +75,15 @@ def scores(q: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
 def eligible(nq: int, nk: int, causal: bool) -> np.ndarray:
     """Boolean [Nq, Nk] matrix: True where key j may be seen by query i.
 
-    Non-causal: every key.  Causal: j <= i (square sequences, query i and key
-    i are the same position).
+    Non-causal: every key.  Causal: j <= i + (nk - nq), the last query aligned
+    with the last key (for square sequences query i and key i are the same
+    position).
     """
     if not causal:
         return np.ones((nq, nk), dtype=bool)
     i = np.arange(nq)[:, None]
     j = np.arange(nk)[None, :]
-    return j <= i
+    return j <= i + (nk - nq)
 
 
 def _masked_scores(q, k, scale, causal):
@@ -123,11 +132,15 @@ def forward_rows(q, k, v, scale, causal, rows):
     """
     out_o = np.empty((len(rows), v.shape[-1]), dtype=np.float64)
     out_l = np.empty(len(rows), dtype=np.float64)
-    n = k.shape[2]
+    nq, nk_all = q.shape[2], k.shape[2]
     for r, (bi, hi, i) in enumerate(rows):
-        nk = (i + 1) if causal else n
-        kk = k[bi, hi, :nk]
-        vv = v[bi, hi, :nk]
+        count = min(i + (nk_all - nq) + 1, nk_all) if causal else nk_all
+        if count <= 0:
+            out_o[r] = 0.0
+            out_l[r] = -np.inf
+            continue
+        kk = k[bi, hi, :count]
+        vv = v[bi, hi, :count]
         s = scale * (kk @ q[bi, hi, i])
         m = s.max()
         w = np.exp(s - m)
@@ -135,6 +148,21 @@ def forward_rows(q, k, v, scale, causal, rows):
         out_o[r] = (w @ vv) / l
         out_l[r] = m + math.log(l)
     return out_o, out_l
+
+
+def forward_varlen(q, k, v, scale, causal, seqlens_q, seqlens_k):
+    """Padded batch: sequence b uses its first seqlens_q[b] query rows and
+    seqlens_k[b] key rows of q [B,H,Nq,d] and k, v [B,H,Nk,d].  Padding rows
+    are O = 0, LSE = -inf.  Returns (O [B,H,Nq,d], LSE [B,H,Nq])."""
+    b, h, nq, _ = q.shape
+    o = np.zeros((b, h, nq, v.shape[-1]), dtype=np.float64)
+    lse = np.full((b, h, nq), -np.inf, dtype=np.float64)
+    for bi in range(b):
+        lq, lk = int(seqlens_q[bi]), int(seqlens_k[bi])
+        for hi in range(h):
+            o[bi, hi, :lq], lse[bi, hi, :lq] = forward_head(q[bi, hi, :lq], k[bi, hi, :lk], v[bi, hi, :lk],
+                                                            scale, causal)
+    return o, lse
 
 
 def backward_head(q, k, v, do, scale, causal, lse=None):
@@ -174,6 +202,23 @@ def backward(q, k, v, do, scale, causal):
         for hi in range(h):
             dq[bi, hi], dk[bi, hi], dv[bi, hi], dd[bi, hi] = backward_head(
                 q[bi, hi], k[bi, hi], v[bi, hi], do[bi, hi], scale, causal)
+    return dq, dk, dv, dd
+
+
+def backward_varlen(q, k, v, do, scale, causal, seqlens_q, seqlens_k):
+    """Gradients of a padded batch (see forward_varlen); padding rows of dQ,
+    dK, dV and D are 0.  Returns (dQ, dK, dV, D)."""
+    b, h, nq, _ = q.shape
+    dq = np.zeros(q.shape, dtype=np.float64)
+    dk = np.zeros(k.shape, dtype=np.float64)
+    dv = np.zeros(v.shape, dtype=np.float64)
+    dd = np.zeros((b, h, nq), dtype=np.float64)
+    for bi in range(b):
+        lq, lk = int(seqlens_q[bi]), int(seqlens_k[bi])
+        for hi in range(h):
+            gq, gk, gv, gd = backward_head(q[bi, hi, :lq], k[bi, hi, :lk], v[bi, hi, :lk], do[bi, hi, :lq],
+                                           scale, causal)
+            dq[bi, hi, :lq], dk[bi, hi, :lk], dv[bi, hi, :lk], dd[bi, hi, :lq] = gq, gk, gv, gd
     return dq, dk, dv, dd
 
 

@@ -164,12 +164,16 @@ def check_forward_rows_agree(ora):
 # ---------------------------------------------------------------- brute force
 
 def _mp_forward(q, k, v, scale, causal):
-    """Definition evaluated entry by entry in 50-digit arithmetic (one head)."""
-    n, d, dv = len(q), len(q[0]), len(v[0])
-    o = [[None] * dv for _ in range(n)]
-    lse = [None] * n
-    for i in range(n):
-        keys = range(i + 1) if causal else range(n)
+    """Definition evaluated entry by entry in 50-digit arithmetic (one head).
+    Causal keys of query i: 0 .. i + (nk - nq), the last query aligned with
+    the last key; a query with no key gets O = 0 and LSE = -inf."""
+    nq, nk, d, dv = len(q), len(k), len(q[0]), len(v[0])
+    o = [[mpmath.mpf(0)] * dv for _ in range(nq)]
+    lse = [mpmath.mpf("-inf")] * nq
+    for i in range(nq):
+        keys = range(max(0, min(i + nk - nq + 1, nk))) if causal else range(nk)
+        if len(keys) == 0:
+            continue
         w = {}
         for j in keys:
             s = mpmath.mpf(0)
@@ -188,24 +192,25 @@ def _to_mp(a):
 
 
 @functools.lru_cache(maxsize=None)
-def _brute(n, d, causal, seed):
+def _brute(nq, nk, d, causal, seed):
     """50-digit forward values and central-difference gradients of
-    sum(O * dO) for one random head."""
+    sum(O * dO) for one random head with nq queries and nk keys."""
     mpmath.mp.dps = 50
-    q, k, v, do = (_bf16_values((n, d), seed + t) for t in range(4))
+    q, do = (_bf16_values((nq, d), seed + t) for t in (0, 3))
+    k, v = (_bf16_values((nk, d), seed + t) for t in (1, 2))
     scale = mpmath.mpf(1) / mpmath.sqrt(d)
     Q, K, V, DO = _to_mp(q), _to_mp(k), _to_mp(v), _to_mp(do)
     o, lse = _mp_forward(Q, K, V, scale, causal)
 
     def f(Q_, K_, V_):
         oo, _ = _mp_forward(Q_, K_, V_, scale, causal)
-        return mpmath.fsum(oo[i][c] * DO[i][c] for i in range(n) for c in range(d))
+        return mpmath.fsum(oo[i][c] * DO[i][c] for i in range(nq) for c in range(d))
 
     h = mpmath.mpf("1e-18")
     grads = []
-    for which in range(3):
-        g = np.zeros((n, d))
-        for i in range(n):
+    for which, rows in ((0, nq), (1, nk), (2, nk)):
+        g = np.zeros((rows, d))
+        for i in range(rows):
             for c in range(d):
                 mats = [[row[:] for row in M] for M in (Q, K, V)]
                 x0 = mats[which][i][c]
@@ -220,24 +225,85 @@ def _brute(n, d, causal, seed):
     return (q, k, v, do, float(scale), o_np, lse_np) + tuple(grads)
 
 
-def _check_brute(ora, n, d, causal, seed):
-    q, k, v, do, scale, o_ref, lse_ref, dq_ref, dk_ref, dv_ref = _brute(n, d, causal, seed)
+def _check_brute(ora, nq, nk, d, causal, seed):
+    q, k, v, do, scale, o_ref, lse_ref, dq_ref, dk_ref, dv_ref = _brute(nq, nk, d, causal, seed)
     o, lse = ora.forward(_head(q), _head(k), _head(v), scale, causal)
     assert np.max(np.abs(o[0, 0] - o_ref)) < 1e-13, np.max(np.abs(o[0, 0] - o_ref))
-    assert np.max(np.abs(lse[0, 0] - lse_ref)) < 1e-13
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lse[0, 0]), fin)
+    assert np.max(np.abs(lse[0, 0][fin] - lse_ref[fin]), initial=0.0) < 1e-13
     dq, dk, dv, _ = ora.backward(_head(q), _head(k), _head(v), _head(do), scale, causal)
     for got, ref in ((dq, dq_ref), (dk, dk_ref), (dv, dv_ref)):
         assert np.max(np.abs(got[0, 0] - ref)) < 1e-12, np.max(np.abs(got[0, 0] - ref))
 
 
 def check_brute_force_4x4(ora):
-    _check_brute(ora, 4, 4, False, 101)
-    _check_brute(ora, 4, 4, True, 201)
+    _check_brute(ora, 4, 4, 4, False, 101)
+    _check_brute(ora, 4, 4, 4, True, 201)
 
 
 def check_brute_force_8x8(ora):
-    _check_brute(ora, 8, 8, False, 301)
-    _check_brute(ora, 8, 8, True, 401)
+    _check_brute(ora, 8, 8, 8, False, 301)
+    _check_brute(ora, 8, 8, 8, True, 401)
+
+
+def check_brute_force_unequal(ora):
+    """Unequal query/key counts, both ways, with the bottom-right causal
+    alignment (and one query row with no key when nq > nk)."""
+    _check_brute(ora, 3, 5, 4, True, 501)
+    _check_brute(ora, 5, 3, 4, True, 601)
+    _check_brute(ora, 3, 5, 4, False, 701)
+
+
+# ---------------------------------------------------------------- alignment
+
+def check_decode_row(ora):
+    """A single query against N keys (decoding) sees every key under the
+    causal mask: it equals the unmasked answer, and the last row of a square
+    causal problem."""
+    q, k, v, _ = _random_case(1, 2, 40, 8, 801)
+    last = q[:, :, -1:, :]
+    oc, lc = ora.forward(last, k, v, 0.3, True)
+    on, ln = ora.forward(last, k, v, 0.3, False)
+    assert np.max(np.abs(oc - on)) < 1e-15 and np.max(np.abs(lc - ln)) < 1e-15
+    osq, lsq = ora.forward(q, k, v, 0.3, True)
+    assert np.max(np.abs(oc[:, :, 0] - osq[:, :, -1])) < 1e-13
+
+
+def check_leading_rows_masked(ora):
+    """With two more queries than keys the first two queries see no key
+    (O = 0, LSE = -inf, no NaN), the third sees key 0 only (O = v_0,
+    LSE = s_00) and the last sees every key."""
+    _, k, v, _ = _random_case(1, 1, 6, 8, 901)
+    q = _random_case(1, 1, 8, 8, 911)[0]
+    o, lse = ora.forward(q, k, v, 0.5, True)
+    assert np.all(o[0, 0, :2] == 0.0) and np.all(lse[0, 0, :2] == -np.inf)
+    assert np.max(np.abs(o[0, 0, 2] - v[0, 0, 0])) < 1e-15
+    s00 = 0.5 * sum(q[0, 0, 2, c] * k[0, 0, 0, c] for c in range(8))
+    assert abs(lse[0, 0, 2] - s00) < 1e-14
+    on, ln = ora.forward(q[:, :, -1:], k, v, 0.5, False)
+    assert np.max(np.abs(o[0, 0, -1] - on[0, 0, 0])) < 1e-13
+    dq, dk, dv, _ = ora.backward(q, k, v, _random_case(1, 1, 8, 8, 921)[0], 0.5, True)
+    assert np.all(dq[0, 0, :2] == 0.0) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+
+
+def check_varlen_slices(ora):
+    """A padded batch equals each sequence computed on its own valid rows;
+    padding rows are O = 0, LSE = -inf and zero gradients."""
+    q = _random_case(3, 2, 9, 4, 1001)[0]
+    k, v = _random_case(3, 2, 7, 4, 1011)[1:3]
+    do = _random_case(3, 2, 9, 4, 1021)[0]
+    sq, sk = [9, 4, 6], [7, 7, 2]
+    for causal in (False, True):
+        o, lse = ora.forward_varlen(q, k, v, 0.4, causal, sq, sk)
+        dq, dk, dv, _ = ora.backward_varlen(q, k, v, do, 0.4, causal, sq, sk)
+        for b in range(3):
+            ob, lb = ora.forward(q[b:b + 1, :, :sq[b]], k[b:b + 1, :, :sk[b]], v[b:b + 1, :, :sk[b]], 0.4, causal)
+            assert np.max(np.abs(o[b, :, :sq[b]] - ob[0]), initial=0.0) < 1e-15
+            assert np.array_equal(lse[b, :, :sq[b]], lb[0])
+            assert np.all(o[b, :, sq[b]:] == 0.0) and np.all(lse[b, :, sq[b]:] == -np.inf)
+            assert np.all(dq[b, :, sq[b]:] == 0.0) and np.all(dk[b, :, sk[b]:] == 0.0)
+            assert np.all(dv[b, :, sk[b]:] == 0.0)
 
 
 # ---------------------------------------------------------------- memory exercise
@@ -268,6 +334,10 @@ ALL_CHECKS = [
     check_forward_rows_agree,
     check_brute_force_4x4,
     check_brute_force_8x8,
+    check_brute_force_unequal,
+    check_decode_row,
+    check_leading_rows_masked,
+    check_varlen_slices,
     check_memory_exercise,
 ]
 

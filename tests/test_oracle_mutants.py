@@ -14,8 +14,8 @@ SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), 
 MUTATIONS = {
     "scale_dropped": ("return scale * (q @ k.T)", "return (q @ k.T)"),
     "operands_transposed": ("return scale * (q @ k.T)", "return scale * (k @ q.T)"),
-    "causal_strict": ("return j <= i", "return j < i"),
-    "causal_flipped": ("return j <= i", "return j >= i"),
+    "causal_strict": ("return j <= i + (nk - nq)", "return j < i + (nk - nq)"),
+    "causal_flipped": ("return j <= i + (nk - nq)", "return j >= i + (nk - nq)"),
     "no_max_shift": ("np.exp(s - m[:, None])", "np.exp(s)"),
     "no_normalisation": ("o = (w @ v) / safe_l[:, None]", "o = (w @ v)"),
     "values_from_keys": ("o = (w @ v) / safe_l[:, None]", "o = (w @ k) / safe_l[:, None]"),
@@ -25,7 +25,10 @@ MUTATIONS = {
     "dk_scale_dropped": ("dk = scale * (ds.T @ q)", "dk = (ds.T @ q)"),
     "dv_transposed": ("dv = p.T @ do", "dv = p @ do"),
     "dq_from_values": ("dq = scale * (ds @ k)", "dq = scale * (ds @ v)"),
-    "rows_off_by_one": ("nk = (i + 1) if causal else n", "nk = max(i, 1) if causal else n"),
+    "rows_off_by_one": ("count = min(i + (nk_all - nq) + 1, nk_all)", "count = min(i + (nk_all - nq), nk_all)"),
+    "causal_offset_flipped": ("return j <= i + (nk - nq)", "return j <= i - (nk - nq)"),
+    "causal_top_left": ("return j <= i + (nk - nq)", "return j <= i"),
+    "varlen_keys_sliced_by_query_length": ("v[bi, hi, :lk],\n                                                            scale", "v[bi, hi, :lq],\n                                                            scale"),
 }
 
 
