@@ -46,8 +46,12 @@ def lib() -> ctypes.CDLL:
         vp, i, f, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_fwd.restype = st
+        L.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_fwd_varlen.restype = st
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd.restype = st
+        L.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_bwd_varlen.restype = st
         L.fa_bwd_stage.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd_stage.restype = st
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
@@ -83,9 +87,21 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: 
     return lib().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
 
 
+def fa_fwd_varlen(q: int, k: int, v: int, o: int, lse: int, seqlens_q: int, seqlens_k: int, B: int, H: int,
+                  Nq: int, Nk: int, d: int, scale: float, causal: int, stream: int) -> int:
+    return lib().fa_fwd_varlen(q, k, v, o, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream)
+
+
 def fa_bwd(q: int, k: int, v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int, workspace: int,
            B: int, H: int, N: int, d: int, scale: float, causal: int, stream: int) -> int:
     return lib().fa_bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, N, d, scale, causal, stream)
+
+
+def fa_bwd_varlen(q: int, k: int, v: int, o: int, lse: int, do: int, dq: int, dk: int, dv: int, workspace: int,
+                  seqlens_q: int, seqlens_k: int, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
+                  causal: int, stream: int) -> int:
+    return lib().fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, workspace, seqlens_q, seqlens_k, B, H, Nq, Nk, d,
+                               scale, causal, stream)
 
 
 def fa_bwd_stage(stage: int, q: int, k: int, v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int,
@@ -167,6 +183,36 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None)
     return o, lse
 
 
+def forward_varlen(q, k, v, seqlens_q=None, seqlens_k=None, causal: bool = False, scale: float | None = None,
+                   out=None):
+    """O, LSE through fa_fwd_varlen: q [B,H,Nq,d], k and v [B,H,Nk,d] (bf16,
+    CUDA); seqlens_q / seqlens_k optional int32 CUDA tensors of B valid
+    lengths.  Causal alignment is bottom-right (see include/fa.h)."""
+    import torch
+    for t in (q, k, v):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v must be contiguous 4-D bf16 CUDA tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, H, Nk, d] with the batch, heads and d of q")
+    for t in (seqlens_q, seqlens_k):
+        if t is not None and (not t.is_cuda or t.dtype != torch.int32 or t.numel() != B or not t.is_contiguous()):
+            raise ValueError("seqlens must be contiguous int32 CUDA tensors of B entries")
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    if out is None:
+        o = torch.empty((B, H, Nq, d), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    _check("fa_fwd_varlen", fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                          seqlens_q.data_ptr() if seqlens_q is not None else 0,
+                                          seqlens_k.data_ptr() if seqlens_k is not None else 0,
+                                          B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    return o, lse
+
+
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, workspace=None,
              out=None):
     """dQ, dK, dV through fa_bwd on the current stream (fp32 outputs)."""
@@ -183,6 +229,38 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
     _check("fa_bwd", fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                             do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws,
                             B, H, N, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    return dq, dk, dv
+
+
+def backward_varlen(q, k, v, o, lse, do, seqlens_q=None, seqlens_k=None, causal: bool = False,
+                    scale: float | None = None, workspace=None, out=None):
+    """dQ, dK, dV through fa_bwd_varlen: q, do, o [B,H,Nq,d], lse [B,H,Nq],
+    k and v [B,H,Nk,d]; seqlens as forward_varlen (fp32 outputs)."""
+    import torch
+    for t in (q, k, v, do):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v, do must be contiguous 4-D bf16 CUDA tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape or do.shape != q.shape:
+        raise ValueError("k, v must be [B, H, Nk, d] and do [B, H, Nq, d]")
+    for t in (seqlens_q, seqlens_k):
+        if t is not None and (not t.is_cuda or t.dtype != torch.int32 or t.numel() != B or not t.is_contiguous()):
+            raise ValueError("seqlens must be contiguous int32 CUDA tensors of B entries")
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    if out is None:
+        dq = torch.empty((B, H, Nq, d), dtype=torch.float32, device=q.device)
+        dk, dv = (torch.empty((B, H, Nk, d), dtype=torch.float32, device=q.device) for _ in range(2))
+    else:
+        dq, dk, dv = out
+    ws = workspace.data_ptr() if workspace is not None else 0
+    _check("fa_bwd_varlen",
+           fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws,
+                         seqlens_q.data_ptr() if seqlens_q is not None else 0,
+                         seqlens_k.data_ptr() if seqlens_k is not None else 0,
+                         B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
     return dq, dk, dv
 
 

@@ -107,17 +107,111 @@ fa_status check_sizes(int B, int H, int N, int d, int causal) {
   return FA_OK;
 }
 
+// n: rows the units tile (query rows for the forward and dQ, keys for dK/dV);
+// n_stream: rows every unit of a head streams through (sizes the L2 groups).
 fa::SchedParams make_sched(int heads, int n, int d, int causal, int grid_cap, long long budget,
-                           int unit_rows = fa::kUnitRows, int cost_grows = 1) {
+                           int unit_rows = fa::kUnitRows, int cost_grows = 1, int n_stream = 0) {
   fa::SchedParams sp;
   sp.heads = heads;
   sp.units_per_head = (n + unit_rows - 1) / unit_rows;
   sp.cost_grows = cost_grows;
-  sp.group_heads = fa::sched_group_heads(heads, n, d, budget > 0 ? budget : kDefaultL2Budget);
+  sp.group_heads =
+      fa::sched_group_heads(heads, n_stream > 0 ? n_stream : n, d, budget > 0 ? budget : kDefaultL2Budget);
   const long long units = static_cast<long long>(heads) * sp.units_per_head;
   sp.grid = static_cast<int>(units < grid_cap ? units : grid_cap);
   sp.causal = causal;
   return sp;
+}
+
+fa_status fwd_common(const void* q, const void* k, const void* v, float* o, float* lse, const int* seqlens_q,
+                     const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                     fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, Nq, d, causal);
+  if (st != FA_OK) return st;
+  st = check_sizes(B, H, Nk, d, causal);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      (seqlens_q && !aligned(seqlens_q, 4)) || (seqlens_k && !aligned(seqlens_k, 4)))
+    return FA_ERR_MISALIGNED;
+  DeviceInfo di;
+  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
+  const int heads = B * H;
+  fa::FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_bf16_map(&a.tm_q, q, heads, Nq, d) || !encode_bf16_map(&a.tm_k, k, heads, Nk, d) ||
+      !encode_bf16_map(&a.tm_v, v, heads, Nk, d))
+    return FA_ERR_LAUNCH;
+  a.o = o;
+  a.lse = lse;
+  a.geom.nq = Nq;
+  a.geom.nk = Nk;
+  a.geom.seqlens_q = seqlens_q;
+  a.geom.seqlens_k = seqlens_k;
+  a.geom.heads_per_batch = H;
+  a.d = d;
+  a.causal = causal;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.sched = make_sched(heads, Nq, d, causal, di.sms, 0, fa::kUnitRows, 1, Nk);
+  a.status = di.status;
+  a.wait_limit_ns = wait_limit_ns();
+  a.stall_unit = test_stall_unit();
+  return fa::launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+// Checks the arguments of a backward call (the workspace only for alignment;
+// it may be null) and fills every field of `a` but the row-term buffer.  q, dO, o, lse, dq: [B*H][Nq] rows; k, v, dk, dv:
+// [B*H][Nk] rows.
+fa_status bwd_prepare(fa::BwdArgs& a, const void* q, const void* k, const void* v, const float* o,
+                      const float* lse, const void* dO, float* dq, float* dk, float* dv, const float* workspace,
+                      const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
+                      int causal) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, Nq, d, causal);
+  if (st != FA_OK) return st;
+  st = check_sizes(B, H, Nk, d, causal);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
+      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) ||
+      (workspace && !aligned(workspace, 4)) || (seqlens_q && !aligned(seqlens_q, 4)) ||
+      (seqlens_k && !aligned(seqlens_k, 4)))
+    return FA_ERR_MISALIGNED;
+  DeviceInfo di;
+  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
+  const int heads = B * H;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_bf16_map(&a.tm_q, q, heads, Nq, d) || !encode_bf16_map(&a.tm_k, k, heads, Nk, d) ||
+      !encode_bf16_map(&a.tm_v, v, heads, Nk, d) || !encode_bf16_map(&a.tm_do, dO, heads, Nq, d))
+    return FA_ERR_LAUNCH;
+  a.o = o;
+  a.lse = lse;
+  a.dout = static_cast<const uint16_t*>(dO);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.heads = heads;
+  a.geom.nq = Nq;
+  a.geom.nk = Nk;
+  a.geom.seqlens_q = seqlens_q;
+  a.geom.seqlens_k = seqlens_k;
+  a.geom.heads_per_batch = H;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  // dK/dV: one unit per 128-key tile, heaviest at the start of the sequence,
+  // streaming the head's queries; dQ: one unit per 128-query tile, heaviest
+  // at the end, streaming the head's keys.
+  a.sched_kv = make_sched(heads, Nk, d, causal, di.sms, 0, fa::kTileRows, 0, Nq);
+  a.sched_q = make_sched(heads, Nq, d, causal, di.sms, 0, fa::kTileRows, 1, Nk);
+  a.grid_kv = a.sched_kv.grid;
+  a.grid_q = a.sched_q.grid;
+  a.grid_pre = 2 * di.sms;
+  a.status = di.status;
+  a.wait_limit_ns = wait_limit_ns();
+  return FA_OK;
 }
 
 }  // namespace
@@ -126,31 +220,13 @@ extern "C" {
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H, int N, int d,
                  float scale, int causal, fa_stream_t stream) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  fa_status st = check_sizes(B, H, N, d, causal);
-  if (st != FA_OK) return st;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
-    return FA_ERR_MISALIGNED;
-  DeviceInfo di;
-  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
-  const int heads = B * H;
-  fa::FwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  if (!encode_bf16_map(&a.tm_q, q, heads, N, d) || !encode_bf16_map(&a.tm_k, k, heads, N, d) ||
-      !encode_bf16_map(&a.tm_v, v, heads, N, d))
-    return FA_ERR_LAUNCH;
-  a.o = o;
-  a.lse = lse;
-  a.n = N;
-  a.d = d;
-  a.causal = causal;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.sched = make_sched(heads, N, d, causal, di.sms, 0);
-  a.status = di.status;
-  a.wait_limit_ns = wait_limit_ns();
-  a.stall_unit = test_stall_unit();
-  return fa::launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  return fwd_common(q, k, v, o, lse, nullptr, nullptr, B, H, N, N, d, scale, causal, stream);
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, float* lse, const int* seqlens_q,
+                        const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                        fa_stream_t stream) {
+  return fwd_common(q, k, v, o, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N) {
@@ -159,59 +235,34 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N) {
   return static_cast<size_t>(B) * H * N * sizeof(float);
 }
 
-fa_status fa_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse, const void* dO,
-                 float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d, float scale,
-                 int causal, fa_stream_t stream) {
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  fa_status st = check_sizes(B, H, N, d, causal);
-  if (st != FA_OK) return st;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
-      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) ||
-      (workspace && !aligned(workspace, 4)))
-    return FA_ERR_MISALIGNED;
-  DeviceInfo di;
-  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
-  const int heads = B * H;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                        const void* dO, float* dq, float* dk, float* dv, float* workspace, const int* seqlens_q,
+                        const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                        fa_stream_t stream) {
   fa::BwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  if (!encode_bf16_map(&a.tm_q, q, heads, N, d) || !encode_bf16_map(&a.tm_k, k, heads, N, d) ||
-      !encode_bf16_map(&a.tm_v, v, heads, N, d) || !encode_bf16_map(&a.tm_do, dO, heads, N, d))
-    return FA_ERR_LAUNCH;
+  fa_status st =
+      bwd_prepare(a, q, k, v, o, lse, dO, dq, dk, dv, workspace, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal);
+  if (st != FA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float* delta = workspace;
   if (!delta) {
-    if (cudaMallocAsync(reinterpret_cast<void**>(&delta), fa_bwd_workspace_bytes(B, H, N), s) != cudaSuccess)
+    if (cudaMallocAsync(reinterpret_cast<void**>(&delta), fa_bwd_workspace_bytes(B, H, Nq), s) != cudaSuccess)
       return FA_ERR_LAUNCH;
   }
-  a.o = o;
-  a.lse = lse;
-  a.dout = static_cast<const uint16_t*>(dO);
-  a.dq = dq;
-  a.dk = dk;
-  a.dv = dv;
   a.delta = delta;
-  a.heads = heads;
-  a.n = N;
-  a.d = d;
-  a.causal = causal;
-  a.scale = scale;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  // dK/dV: one unit per 128-key tile, heaviest at the start of the sequence;
-  // dQ: one unit per 128-query tile, heaviest at the end.
-  a.sched_kv = make_sched(heads, N, d, causal, di.sms, 0, fa::kTileRows, 0);
-  a.sched_q = make_sched(heads, N, d, causal, di.sms, 0, fa::kTileRows, 1);
-  a.grid_kv = a.sched_kv.grid;
-  a.grid_q = a.sched_q.grid;
-  a.grid_pre = 2 * di.sms;
-  a.status = di.status;
-  a.wait_limit_ns = wait_limit_ns();
   cudaError_t e = fa::launch_bwd(a, s);
   if (!workspace) {
     cudaError_t e2 = cudaFreeAsync(delta, s);
     if (e == cudaSuccess) e = e2;
   }
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse, const void* dO,
+                 float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d, float scale,
+                 int causal, fa_stream_t stream) {
+  return fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, workspace, nullptr, nullptr, B, H, N, N, d, scale, causal,
+                       stream);
 }
 
 // Scratch of fa_bwd_noalloc: the backward row term D for up to
@@ -227,19 +278,13 @@ static float* g_noalloc_ptr[kMaxDevices];
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const float* o, const float* lse,
                          const void* dO, float* dq, float* dk, float* dv, int B, int H, int N, int d, float scale,
                          int causal, fa_stream_t stream) {
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  fa_status st = check_sizes(B, H, N, d, causal);
+  fa::BwdArgs a;
+  fa_status st =
+      bwd_prepare(a, q, k, v, o, lse, dO, dq, dk, dv, nullptr, nullptr, nullptr, B, H, N, N, d, scale, causal);
   if (st != FA_OK) return st;
   if (static_cast<long long>(B) * H * N > FA_NOALLOC_MAX_ROWS) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
-      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
-    return FA_ERR_MISALIGNED;
-  DeviceInfo di;
-  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
-  float* delta = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     if (!g_noalloc_ptr[dev]) {
@@ -247,76 +292,20 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const floa
       if (cudaGetSymbolAddress(&p, g_fa_noalloc_delta) != cudaSuccess || !p) return FA_ERR_LAUNCH;
       g_noalloc_ptr[dev] = static_cast<float*>(p);
     }
-    delta = g_noalloc_ptr[dev];
+    a.delta = g_noalloc_ptr[dev];  // every row is written by the preprocess kernel before it is read
   }
-  const int heads = B * H;
-  fa::BwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  if (!encode_bf16_map(&a.tm_q, q, heads, N, d) || !encode_bf16_map(&a.tm_k, k, heads, N, d) ||
-      !encode_bf16_map(&a.tm_v, v, heads, N, d) || !encode_bf16_map(&a.tm_do, dO, heads, N, d))
-    return FA_ERR_LAUNCH;
-  a.o = o;
-  a.lse = lse;
-  a.dout = static_cast<const uint16_t*>(dO);
-  a.dq = dq;
-  a.dk = dk;
-  a.dv = dv;
-  a.delta = delta;  // every row is written by the preprocess kernel before it is read
-  a.heads = heads;
-  a.n = N;
-  a.d = d;
-  a.causal = causal;
-  a.scale = scale;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.sched_kv = make_sched(heads, N, d, causal, di.sms, 0, fa::kTileRows, 0);
-  a.sched_q = make_sched(heads, N, d, causal, di.sms, 0, fa::kTileRows, 1);
-  a.grid_kv = a.sched_kv.grid;
-  a.grid_q = a.sched_q.grid;
-  a.grid_pre = 2 * di.sms;
-  a.status = di.status;
-  a.wait_limit_ns = wait_limit_ns();
   return fa::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const float* o, const float* lse,
                        const void* dO, float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d,
                        float scale, int causal, fa_stream_t stream) {
-  if (stage < 0 || stage > 2) return FA_ERR_INVALID_ARG;
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
-  fa_status st = check_sizes(B, H, N, d, causal);
-  if (st != FA_OK) return st;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(dO, 16) ||
-      !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) || !aligned(workspace, 4))
-    return FA_ERR_MISALIGNED;
-  DeviceInfo di;
-  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
-  const int heads = B * H;
+  if (stage < 0 || stage > 2 || !workspace) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a;
-  std::memset(&a, 0, sizeof(a));
-  if (!encode_bf16_map(&a.tm_q, q, heads, N, d) || !encode_bf16_map(&a.tm_k, k, heads, N, d) ||
-      !encode_bf16_map(&a.tm_v, v, heads, N, d) || !encode_bf16_map(&a.tm_do, dO, heads, N, d))
-    return FA_ERR_LAUNCH;
-  a.o = o;
-  a.lse = lse;
-  a.dout = static_cast<const uint16_t*>(dO);
-  a.dq = dq;
-  a.dk = dk;
-  a.dv = dv;
+  fa_status st =
+      bwd_prepare(a, q, k, v, o, lse, dO, dq, dk, dv, workspace, nullptr, nullptr, B, H, N, N, d, scale, causal);
+  if (st != FA_OK) return st;
   a.delta = workspace;
-  a.heads = heads;
-  a.n = N;
-  a.d = d;
-  a.causal = causal;
-  a.scale = scale;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.sched_kv = make_sched(heads, N, d, causal, di.sms, 0, fa::kTileRows, 0);
-  a.sched_q = make_sched(heads, N, d, causal, di.sms, 0, fa::kTileRows, 1);
-  a.grid_kv = a.sched_kv.grid;
-  a.grid_q = a.sched_q.grid;
-  a.grid_pre = 2 * di.sms;
-  a.status = di.status;
-  a.wait_limit_ns = wait_limit_ns();
   return fa::launch_bwd_stage(a, stage, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
                                                                                               : FA_ERR_LAUNCH;
 }

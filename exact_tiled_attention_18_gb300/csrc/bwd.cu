@@ -27,6 +27,7 @@
 
 #include <type_traits>
 
+#include "geom.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -160,18 +161,12 @@ constexpr int kKvOtherRegs = 120;
 static_assert(2 * 128 * kKvEwRegs + 128 * kKvOtherRegs <= kKvThreads * kKvLaunchRegs,
               "register split exceeds the launch allocation");
 
-// Query tiles that see key tile j.
-__device__ __forceinline__ void kv_range(int j, int nt, bool causal, int& i0, int& i1) {
-  i0 = causal ? j : 0;
-  i1 = nt;
-}
-
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kKvThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const float* __restrict__ lse, const float* __restrict__ delta, float* __restrict__ dk,
-                float* __restrict__ dv, const int n, const float scale, const float scale_log2,
+                float* __restrict__ dv, const SeqGeom geom, const float scale, const float scale_log2,
                 const SchedParams sp, int* status, const unsigned long long limit_ns) {
   using L = KvLayout<D>;
   constexpr int S = L::kStages;
@@ -216,7 +211,6 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, status, limit_ns};
-  const int nt = (n + kTileRows - 1) / kTileRows;
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
 
   if (warp < 8) {
@@ -231,8 +225,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     int head, j;
     bool ok = true;
     while (ok && sched_next(it, sp, blockIdx.x, head, j)) {
+      const HeadLen hl = head_len(geom, head);
       int i0, i1;
-      kv_range(j, nt, CAUSAL, i0, i1);
+      key_tile_queries(hl, j, CAUSAL, i0, i1);
       const int unit = head * sp.units_per_head + j;
       for (int i = i0; i < i1; ++i) {
         const uint32_t ls = ldn % S;
@@ -244,16 +239,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tc_fence_after();
         const float* l2s = ld_base + ls * 256;
         const float* dds = l2s + 128;
-        const bool diag = CAUSAL && (i == j);
-        const bool need_mask = diag;
+        // key j*128 + r is hidden from query column c iff c < mlim
+        const bool need_mask = CAUSAL && tile_crosses_diagonal(hl, i, j);
+        const int mlim = r + (j - i) * kTileRows - hl.off;
         const uint64_t c2 = f2_pack(scale_log2, scale_log2);
         // Phase 1: P^T for 32 query columns starting at col0, kept in sr as fp32
-        // bits and packed to bf16 in pk.  MASKED: diagonal tile, where a key
-        // may come after the query.
+        // bits and packed to bf16 in pk.  MASKED: a tile crossing the causal
+        // boundary, where a key may come after the query.
         auto pchunk = [&](auto masked, uint32_t (&sr)[32], int col0, uint32_t (&pk)[16]) {
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
-            // l2s holds -LSE*log2(e) (-inf past the sequence end)
+            // l2s holds -LSE*log2(e) (-inf for padding and key-less queries)
             const float4 l4 = *reinterpret_cast<const float4*>(l2s + col0 + c);
             float p[4];
             f2_unpack(ffma2(f2_from(sr[c], sr[c + 1]), c2, f2_pack(l4.x, l4.y)), p[0], p[1]);
@@ -261,7 +257,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               p[e] = ex2_approx(p[e]);
-              if (decltype(masked)::value && (col0 + c + e) < r) p[e] = 0.f;  // query before key: masked
+              if (decltype(masked)::value && (col0 + c + e) < mlim) p[e] = 0.f;  // key after the query
               sr[c + e] = __float_as_uint(p[e]);
             }
             pk[c / 2] = pack_bf16x2(p[0], p[1]);
@@ -325,21 +321,37 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         ++ldn;
       }
       if (!ok) break;
-      // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
+      // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK; key
+      // rows past the valid length (and tiles no query sees) get zeros
+      const int row = j * kTileRows + r;
+      const bool valid = row < geom.nk;
+      float* dst = (w == 0 ? dv : dk) + (static_cast<size_t>(head) * geom.nk + row) * D;
+      if (i0 == i1) {
+        if (valid) {
+          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+          for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = z;
+        }
+        continue;
+      }
       ok = warp_wait(BAR(L::ACC_FULL), an & 1, wc, SITE_KV_EW_ACC, unit);
       if (!ok) break;
       ++an;
       tc_fence_after();
-      const int row = j * kTileRows + r;
-      const bool valid = row < n;
-      float* dst = (w == 0 ? dv : dk) + (static_cast<size_t>(head) * n + row) * D;
       const uint32_t col = (w == 0) ? L::kColDV : L::kColDK;
       const float mul = (w == 0) ? 1.0f : scale;
+      // a padding key row may have met scores far above its queries' LSE:
+      // select zeros rather than scale what it accumulated
+      const bool live = row < hl.lk;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + col + 32 * c, v);
         tmem_ld_wait();
+        if (!live) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
         if (valid) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -366,7 +378,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       bool ok = true;
       while (ok && sched_next(it, sp, blockIdx.x, head, j)) {
         int i0, i1;
-        kv_range(j, nt, CAUSAL, i0, i1);
+        key_tile_queries(head_len(geom, head), j, CAUSAL, i0, i1);
+        if (i0 == i1) continue;
         const int unit = head * sp.units_per_head + j;
         ok = wait_bounded(BAR(L::KV_EMPTY), (kvn & 1) ^ 1, wc, SITE_KV_LOAD_KV, unit);
         if (!ok) break;
@@ -415,7 +428,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       bool ok = true;
       while (ok && sched_next(it, sp, blockIdx.x, head, j)) {
         int i0, i1;
-        kv_range(j, nt, CAUSAL, i0, i1);
+        key_tile_queries(head_len(geom, head), j, CAUSAL, i0, i1);
+        if (i0 == i1) continue;
         const int unit = head * sp.units_per_head + j;
         ok = wait_bounded(BAR(L::KV_FULL), kvn & 1, wc, SITE_KV_MMA_KV, unit);
         if (!ok) break;
@@ -489,11 +503,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     int head, j;
     bool ok = true;
     while (ok && sched_next(it, sp, blockIdx.x, head, j)) {
+      const HeadLen hl = head_len(geom, head);
       int i0, i1;
-      kv_range(j, nt, CAUSAL, i0, i1);
+      key_tile_queries(hl, j, CAUSAL, i0, i1);
       const int unit = head * sp.units_per_head + j;
-      lse_h = lse + static_cast<size_t>(head) * n;
-      const float* d_h = delta + static_cast<size_t>(head) * n;
+      lse_h = lse + static_cast<size_t>(head) * geom.nq;
+      const float* d_h = delta + static_cast<size_t>(head) * geom.nq;
       for (int i = i0; i < i1; ++i) {
         const uint32_t ls = ldn % S;
         ok = warp_wait(BAR(L::LD_EMPTY + ls), ((ldn / S) & 1) ^ 1, wc, SITE_KV_LD_EMPTY, unit);
@@ -503,8 +518,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         for (int t = 0; t < 4; ++t) {
           const int idx = lane * 4 + t;
           const int q = i * kTileRows + idx;
-          const bool in = q < n;
-          l2s[idx] = in ? -lse_h[q] * kLog2e : -CUDART_INF_F;
+          const float lv = q < hl.lq ? lse_h[q] : -CUDART_INF_F;
+          const bool in = lv > -CUDART_INF_F;  // a valid query with at least one key
+          l2s[idx] = in ? -lv * kLog2e : -CUDART_INF_F;
           l2s[128 + idx] = in ? d_h[q] : 0.f;
         }
         mbar_arrive_warp(BAR(L::LD_FULL + ls));
@@ -560,7 +576,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kQThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              const float* __restrict__ lse, float* __restrict__ delta, float* __restrict__ dq, const int n,
+              const float* __restrict__ lse, float* __restrict__ delta, float* __restrict__ dq, const SeqGeom geom,
               const float scale, const float scale_log2, const SchedParams sp, int* status,
               const unsigned long long limit_ns) {
   using L = QLayout<D>;
@@ -604,7 +620,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, status, limit_ns};
-  const int nt = (n + kTileRows - 1) / kTileRows;
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
 
   if (warp < 8) {
@@ -625,12 +640,27 @@ __global__ void __launch_bounds__(kQThreads, 1)
     int head, i;
     bool ok = true;
     while (ok && sched_next(it, sp, blockIdx.x, head, i)) {
-      const int nk = CAUSAL ? min(i + 1, nt) : nt;
+      const HeadLen hl = head_len(geom, head);
+      const int nk = query_tile_keys(hl, i, CAUSAL);
       const int unit = head * sp.units_per_head + i;
       const int row = i * kTileRows + r;
-      const bool valid = row < n;
-      const float l2 = valid ? lse[static_cast<size_t>(head) * n + row] * kLog2e : CUDART_INF_F;
-      const float dd = valid ? delta[static_cast<size_t>(head) * n + row] : 0.f;
+      const bool valid = row < geom.nq;
+      const size_t ridx = static_cast<size_t>(head) * geom.nq + row;
+      float* dst = dq + ridx * D;
+      if (nk == 0) {
+        // padding rows, or rows that see no key: zero gradient and row term
+        if (valid) {
+          const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+          for (int c = w * (D / 2); c < (w + 1) * (D / 2); c += 4) *reinterpret_cast<float4*>(dst + c) = z;
+          if (w == 0) delta[ridx] = 0.f;
+        }
+        continue;
+      }
+      const float lv = row < hl.lq ? lse[ridx] : -CUDART_INF_F;
+      const bool has = lv > -CUDART_INF_F;  // a valid row with at least one key
+      const float l2 = has ? lv * kLog2e : CUDART_INF_F;
+      const float dd = has ? delta[ridx] : 0.f;
       const float nl2 = -l2;
       const uint64_t c2 = f2_pack(scale_log2, scale_log2);
       const uint64_t nl2x2 = f2_pack(nl2, nl2);
@@ -641,12 +671,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (!ok) break;
         ++sn;
         tc_fence_after();
-        const bool diag = CAUSAL && (jt == i);
-        const bool tail = (jt == nt - 1) && ((n & (kTileRows - 1)) != 0);
+        const bool diag = CAUSAL && tile_crosses_diagonal(hl, i, jt);
+        const bool tail = (jt == hl.nkt - 1) && ((hl.lk & (kTileRows - 1)) != 0);
         // number of eligible key columns of this tile for this row
         const bool need_mask = diag || tail;
-        const int lim = need_mask ? ((CAUSAL ? min(row + 1, n) : n) - jt * kTileRows) : kTileRows;
-        // MASKED: diagonal or tail tile, where some key columns are not eligible
+        const int lim = need_mask ? ((CAUSAL ? min(row + hl.off + 1, hl.lk) : hl.lk) - jt * kTileRows) : kTileRows;
+        // MASKED: a tile crossing the causal boundary or holding the last
+        // valid key, where some key columns are not eligible
         auto chunk = [&](auto masked, const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&pk)[16],
                          uint32_t (&hk)[16], uint32_t (&lk)[16]) {
           uint64_t acc = f2_pack(0.f, 0.f);
@@ -707,9 +738,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
       if (!ok) break;
       ++an;
       tc_fence_after();
-      if (w == 0 && valid) delta[static_cast<size_t>(head) * n + row] = dd + dlt;
+      if (w == 0 && valid) delta[ridx] = has ? dd + dlt : 0.f;
       // warpgroup w writes dQ columns [w d/2, (w+1) d/2)
-      float* dst = dq + (static_cast<size_t>(head) * n + row) * D;
+      const float mul = has ? scale : 0.f;
 #pragma unroll 1
       for (int c = w * (D / 64); c < (w + 1) * (D / 64); ++c) {
         uint32_t v[32], bv[32];
@@ -720,10 +751,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             float4 o4;
-            o4.x = (__uint_as_float(v[4 * e + 0]) - dlt * __uint_as_float(bv[4 * e + 0])) * scale;
-            o4.y = (__uint_as_float(v[4 * e + 1]) - dlt * __uint_as_float(bv[4 * e + 1])) * scale;
-            o4.z = (__uint_as_float(v[4 * e + 2]) - dlt * __uint_as_float(bv[4 * e + 2])) * scale;
-            o4.w = (__uint_as_float(v[4 * e + 3]) - dlt * __uint_as_float(bv[4 * e + 3])) * scale;
+            o4.x = (__uint_as_float(v[4 * e + 0]) - dlt * __uint_as_float(bv[4 * e + 0])) * mul;
+            o4.y = (__uint_as_float(v[4 * e + 1]) - dlt * __uint_as_float(bv[4 * e + 1])) * mul;
+            o4.z = (__uint_as_float(v[4 * e + 2]) - dlt * __uint_as_float(bv[4 * e + 2])) * mul;
+            o4.w = (__uint_as_float(v[4 * e + 3]) - dlt * __uint_as_float(bv[4 * e + 3])) * mul;
             *reinterpret_cast<float4*>(dst + 32 * c + 4 * e) = o4;
           }
         }
@@ -741,7 +772,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
       int head, i;
       bool ok = true;
       while (ok && sched_next(it, sp, blockIdx.x, head, i)) {
-        const int nk = CAUSAL ? min(i + 1, nt) : nt;
+        const int nk = query_tile_keys(head_len(geom, head), i, CAUSAL);
+        if (nk == 0) continue;
         const int unit = head * sp.units_per_head + i;
         ok = wait_bounded(BAR(L::Q_EMPTY), (qn & 1) ^ 1, wc, SITE_Q_LOAD_Q, unit);
         if (!ok) break;
@@ -789,7 +821,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
       int head, i;
       bool ok = true;
       while (ok && sched_next(it, sp, blockIdx.x, head, i)) {
-        const int nk = CAUSAL ? min(i + 1, nt) : nt;
+        const int nk = query_tile_keys(head_len(geom, head), i, CAUSAL);
+        if (nk == 0) continue;
         const int unit = head * sp.units_per_head + i;
         ok = wait_bounded(BAR(L::Q_FULL), qn & 1, wc, SITE_Q_MMA_Q, unit);
         if (!ok) break;
@@ -864,7 +897,7 @@ template <int D, bool CAUSAL>
 cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
   if (stage == 0) {
-    preprocess_kernel<D><<<a.grid_pre, 256, 0, stream>>>(a.o, a.dout, a.delta, a.heads * a.n);
+    preprocess_kernel<D><<<a.grid_pre, 256, 0, stream>>>(a.o, a.dout, a.delta, a.heads * a.geom.nq);
   } else if (stage == 1) {
     // dQ first: it turns D' = rowsum(dO o O) into the exact row term
     using L = QLayout<D>;
@@ -876,7 +909,7 @@ cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<a.grid_q, kQThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dq,
-                                                         a.n, a.scale, a.scale_log2, a.sched_q, a.status,
+                                                         a.geom, a.scale, a.scale_log2, a.sched_q, a.status,
                                                          a.wait_limit_ns);
   } else {
     using L = KvLayout<D>;
@@ -889,7 +922,7 @@ cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
     kern<<<a.grid_kv, kKvThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dk,
-                                                           a.dv, a.n, a.scale, a.scale_log2, a.sched_kv, a.status,
+                                                           a.dv, a.geom, a.scale, a.scale_log2, a.sched_kv, a.status,
                                                            a.wait_limit_ns);
   }
   return cudaGetLastError();

@@ -32,6 +32,7 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include "geom.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -84,14 +85,23 @@ struct FwdLayout {
   static constexpr uint32_t kColO = 256;
 };
 
-__device__ __forceinline__ void unit_tiles(int pair, int nkt, bool causal, int& na, int& nb) {
-  if (causal) {
-    na = min(2 * pair + 1, nkt);
-    nb = min(2 * pair + 2, nkt);
-  } else {
-    na = nkt;
-    nb = nkt;
-  }
+// Valid lengths and key-tile counts of one work unit (a head and its query
+// tiles 2*pair and 2*pair+1); a count of 0 means the tile has nothing to
+// compute (all padding, or no eligible key).
+struct UnitGeom {
+  int lq, lk, off, nkt, na, nb;
+};
+
+__device__ __forceinline__ UnitGeom unit_geom(const SeqGeom& g, int head, int pair, bool causal) {
+  const HeadLen h = head_len(g, head);
+  UnitGeom u;
+  u.lq = h.lq;
+  u.lk = h.lk;
+  u.off = h.off;
+  u.nkt = h.nkt;
+  u.na = query_tile_keys(h, 2 * pair, causal);
+  u.nb = query_tile_keys(h, 2 * pair + 1, causal);
+  return u;
 }
 
 // Wait with every lane of the warp and agree on the outcome, so that the
@@ -115,7 +125,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, float* __restrict__ o, float* __restrict__ lse,
-               const int n, const float scale_log2, const SchedParams sp, int* status,
+               const SeqGeom geom, const float scale_log2, const SchedParams sp, int* status,
                const unsigned long long limit_ns, const int stall_unit) {
   using L = FwdLayout<D>;
   constexpr int S = L::kSlots;
@@ -159,7 +169,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, status, limit_ns};
-  const int nkt = (n + kTileRows - 1) / kTileRows;
+  const int nq = geom.nq;
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
 
   if (warp < 8) {
@@ -175,13 +185,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     int head, pair;
     bool ok = true;
     while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
-      int na, nb;
-      unit_tiles(pair, nkt, CAUSAL, na, nb);
-      const int nt = t ? nb : na;
+      const UnitGeom u = unit_geom(geom, head, pair, CAUSAL);
+      const int nt = t ? u.nb : u.na;
       const int qtile = 2 * pair + t;
       const int row = qtile * kTileRows + r;
       const int unit = head * sp.units_per_head + pair;
       float m_ref = 0.f, l = 0.f;
+      if (nt == 0) {
+        // no key for any row of this tile (or all padding): O = 0, LSE = -inf
+        if (row < nq) {
+          float* orow = o + (static_cast<size_t>(head) * nq + row) * D;
+#pragma unroll 1
+          for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+          lse[static_cast<size_t>(head) * nq + row] = -CUDART_INF_F;
+        }
+        continue;
+      }
       for (int j = 0; j < nt; ++j) {
         ok = warp_wait(BAR(L::S_FULL + t), sn & 1, wc, SITE_SOFTMAX_S, unit);
         if (!ok) break;
@@ -194,10 +213,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-        const bool diag = CAUSAL && (j == qtile);
-        const bool tail = (j == nkt - 1) && ((n & (kTileRows - 1)) != 0);
-        if (diag || tail) {
-          const int lim = (CAUSAL ? min(row + 1, n) : n) - j * kTileRows;
+        // keys past the valid length, or (causal) past the row's last key; a
+        // padding row masks every key, so that it never takes part in the
+        // warp's rescale vote and its values cannot change valid rows' rounding
+        const bool diag = CAUSAL && (j * kTileRows + kTileRows - 1 > qtile * kTileRows + u.off);
+        const bool tail = (j == u.nkt - 1) && ((u.lk & (kTileRows - 1)) != 0);
+        const bool padq = qtile * kTileRows + kTileRows > u.lq;
+        if (diag || tail || padq) {
+          const int lim = row < u.lq ? (CAUSAL ? min(row + u.off + 1, u.lk) : u.lk) - j * kTileRows : 0;
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -CUDART_INF_F;
         }
@@ -272,14 +295,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (!ok) break;
       ++on;
       tc_fence_after();
-      const float inv = l > 0.f ? 1.0f / l : 0.f;
-      const bool valid = row < n;
-      float* orow = o + (static_cast<size_t>(head) * n + row) * D;
+      // rows past the valid length are padding and rows without an eligible
+      // key have l = 0: both get O = 0, LSE = -inf (selected, so that what a
+      // padding row accumulated never reaches the output)
+      const bool live = l > 0.f && row < u.lq;
+      const float inv = live ? 1.0f / l : 0.f;
+      const bool valid = row < nq;
+      float* orow = o + (static_cast<size_t>(head) * nq + row) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tO + 32 * c, v);
         tmem_ld_wait();
+        if (!live) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
         if (valid) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -292,7 +323,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
       }
-      if (valid) lse[static_cast<size_t>(head) * n + row] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -CUDART_INF_F;
+      if (valid)
+        lse[static_cast<size_t>(head) * nq + row] =
+            live ? (m_ref + log2f(l)) * kLn2 : -CUDART_INF_F;
     }
   } else {
    regs_decrease<kFwdOtherRegs>();
@@ -306,8 +339,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int head, pair;
       bool ok = true;
       while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
-        int na, nb;
-        unit_tiles(pair, nkt, CAUSAL, na, nb);
+        const UnitGeom u = unit_geom(geom, head, pair, CAUSAL);
+        const int nmax = max(u.na, u.nb);
+        if (nmax == 0) continue;  // nothing to compute for this unit
         const int unit = head * sp.units_per_head + pair;
         ok = wait_bounded(BAR(L::Q_EMPTY), (qn & 1) ^ 1, wc, SITE_LOAD_Q, unit);
         if (!ok) break;
@@ -319,7 +353,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int kb = 0; kb < D / 64; ++kb)
             tma_load_3d_hint(sbase + L::kQOff + t * L::kTileBytes + kb * 16384, &tm_q, BAR(L::Q_FULL), kb * 64,
                              (2 * pair + t) * kTileRows, head, pol_q);
-        for (int j = 0; j < nb && ok; ++j) {
+        for (int j = 0; j < nmax && ok; ++j) {
 #pragma unroll 1
           for (int w = 0; w < 2; ++w) {
             const uint32_t slot = kvpos % S, use = kvpos / S;
@@ -381,8 +415,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int head, pair;
       bool ok = true;
       while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
-        int na, nb;
-        unit_tiles(pair, nkt, CAUSAL, na, nb);
+        const UnitGeom u = unit_geom(geom, head, pair, CAUSAL);
+        const int na = u.na, nb = u.nb, nmax = max(na, nb);
+        if (nmax == 0) continue;  // nothing to compute for this unit
         const int unit = head * sp.units_per_head + pair;
         ok = wait_bounded(BAR(L::Q_FULL), qn & 1, wc, SITE_MMA_Q, unit);
         if (!ok) break;
@@ -390,15 +425,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ok = wait_bounded(BAR(L::KV_FULL + kvbase % S), (kvbase / S) & 1, wc, SITE_MMA_KV, unit);
         if (!ok) break;
         tc_fence_after();
-        issue_s(0, slot_addr(kvbase));
-        umma_commit(BAR(L::S_FULL + 0));
-        issue_s(1, slot_addr(kvbase));
-        umma_commit(BAR(L::S_FULL + 1));
-        for (int j = 0; j < nb; ++j) {
+        if (na > 0) {
+          issue_s(0, slot_addr(kvbase));
+          umma_commit(BAR(L::S_FULL + 0));
+        }
+        if (nb > 0) {
+          issue_s(1, slot_addr(kvbase));
+          umma_commit(BAR(L::S_FULL + 1));
+        }
+        for (int j = 0; j < nmax; ++j) {
           const uint32_t kpos = kvbase + 2 * j, vpos = kpos + 1, knext = kpos + 2;
-          const bool has_a = j < na, next_a = j + 1 < na, next_b = j + 1 < nb;
-          umma_commit(BAR(L::KV_EMPTY + kpos % S));  // K_j is free once S_B(j) completes
-          if (!next_b) umma_commit(BAR(L::Q_EMPTY));  // the unit's last S has been issued
+          const bool has_a = j < na, next_a = j + 1 < na, has_b = j < nb, next_b = j + 1 < nb;
+          umma_commit(BAR(L::KV_EMPTY + kpos % S));  // K_j is free once S(j) of both tiles completes
+          if (!next_a && !next_b) umma_commit(BAR(L::Q_EMPTY));  // the unit's last S has been issued
           ok = wait_bounded(BAR(L::KV_FULL + vpos % S), (vpos / S) & 1, wc, SITE_MMA_KV, unit);
           if (!ok) break;
           if (has_a) {
@@ -416,13 +455,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               umma_commit(BAR(L::S_FULL + 0));
             }
           }
-          ok = wait_bounded(BAR(L::P_FULL + 1), pn1 & 1, wc, SITE_MMA_P, unit);
-          if (!ok) break;
-          ++pn1;
-          tc_fence_after();
-          issue_pv(1, slot_addr(vpos), j > 0);
-          if (!next_b) umma_commit(BAR(L::O_FULL + 1));
-          umma_commit(BAR(L::KV_EMPTY + vpos % S));  // V_j is free once PV_B(j) completes
+          if (has_b) {
+            ok = wait_bounded(BAR(L::P_FULL + 1), pn1 & 1, wc, SITE_MMA_P, unit);
+            if (!ok) break;
+            ++pn1;
+            tc_fence_after();
+            issue_pv(1, slot_addr(vpos), j > 0);
+            if (!next_b) umma_commit(BAR(L::O_FULL + 1));
+          }
+          umma_commit(BAR(L::KV_EMPTY + vpos % S));  // V_j is free once PV(j) of both tiles completes
           if (next_b) {
             ok = wait_bounded(BAR(L::KV_FULL + knext % S), (knext / S) & 1, wc, SITE_MMA_KV, unit);
             if (!ok) break;
@@ -431,7 +472,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             umma_commit(BAR(L::S_FULL + 1));
           }
         }
-        kvbase += 2 * nb;
+        kvbase += 2 * nmax;
       }
       // every MMA this thread issued completes before tensor memory is freed
       umma_commit(BAR(L::DRAIN));
@@ -460,7 +501,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   if (fattr.numRegs != kFwdLaunchRegs) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<a.sched.grid, kFwdThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.n,
+  kern<<<a.sched.grid, kFwdThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.geom,
                                                              a.scale_log2, a.sched, a.status, a.wait_limit_ns,
                                                              a.stall_unit);
   return cudaGetLastError();

@@ -10,11 +10,20 @@
 
 namespace fa {
 
+// Sequence geometry: padded query/key lengths and optional per-sequence valid
+// lengths (device arrays of B ints; null means all rows are valid).
+struct SeqGeom {
+  int nq, nk;
+  const int* seqlens_q;
+  const int* seqlens_k;
+  int heads_per_batch;  // H: head index / H = sequence index
+};
+
 struct FwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [B*H][N][d] bf16, box 64 x 128 x 1, 128-byte swizzle
-  float* o;                      // [B*H][N][d] fp32
-  float* lse;                    // [B*H][N] fp32
-  int n;                         // sequence length
+  CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [B*H][Nq or Nk][d] bf16, box 64 x 128 x 1, 128-byte swizzle
+  float* o;                      // [B*H][Nq][d] fp32
+  float* lse;                    // [B*H][Nq] fp32
+  SeqGeom geom;
   int d;                         // head dimension (64 or 128)
   int causal;
   float scale_log2;              // softmax scale * log2(e)
@@ -34,9 +43,9 @@ struct BwdArgs {
   float* dq;
   float* dk;
   float* dv;
-  float* delta;                         // D_i = rowsum(dO * O), [B*H][N]
+  float* delta;                         // D_i = rowsum(dO * O), [B*H][Nq]
   int heads;
-  int n;
+  SeqGeom geom;
   int d;
   int causal;
   float scale;

@@ -20,7 +20,8 @@
  * ---------------------------------------
  *  - Layout: every tensor is contiguous row-major [B][H][N][d]; the
  *    log-sum-exp and the backward row term are [B][H][N].  One (b, h) pair
- *    is one head; queries and keys have the same length N.
+ *    is one head; queries and keys have the same length N (the _varlen
+ *    calls take separate query and key lengths and per-sequence lengths).
  *  - Types: Q, K, V and dO are bf16 (raw 16-bit storage, `const void*`);
  *    O, LSE, dQ, dK, dV and the workspace are fp32.
  *  - Mask: causal = 0 means no mask; causal = 1 means query i sees key j iff
@@ -85,6 +86,31 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, float* o, float* l
                  float scale, int causal, fa_stream_t stream);
 
 /*
+ * Forward pass over unequal query/key lengths and padded batches.
+ *   q       : bf16 [B][H][Nq][d];  k, v : bf16 [B][H][Nk][d].
+ *   o, lse  : fp32 [B][H][Nq][d] and [B][H][Nq].
+ *   seqlens_q, seqlens_k : device arrays of B ints, the valid lengths of
+ *             each sequence (values clamped to [0, Nq] and [0, Nk]); rows past
+ *             them are padding.  NULL means every row is valid.
+ * Sequence b uses its first Lq = seqlens_q[b] queries and Lk = seqlens_k[b]
+ * keys.  Causal alignment is bottom-right: query i sees key j iff
+ * j <= i + (Lk - Lq), so the last query sits at the last key -- the reading
+ * of "FlashAttention Interview Questions ...", section "Does subtracting the
+ * maximum solve every numerical issue?", which warns that unequal lengths,
+ * padding and packed sequences need an explicit alignment.  With Lq = Lk it
+ * is the square rule of fa_fwd; a single query (decoding) sees every key.
+ * Rows with no eligible key and padding rows are written as O = 0,
+ * LSE = -inf.  Padding rows of q, k and v do not affect the result as long as
+ * their values are below 1e18 in magnitude (so that every dot product stays
+ * finite in fp32).  fa_fwd(...) equals
+ * fa_fwd_varlen(..., NULL, NULL, B, H, N, N, ...).  Errors and conventions
+ * as fa_fwd; seqlens pointers must be 4-byte aligned.
+ */
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, float* lse, const int* seqlens_q,
+                        const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                        fa_stream_t stream);
+
+/*
  * Backward pass by recomputation: attention probabilities are rebuilt from
  * q, k and the saved lse instead of being stored ("FlashAttention Interview
  * Questions ...", section "Why can recomputation help training?").
@@ -103,6 +129,26 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, float* o, float* l
 fa_status fa_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse, const void* dO,
                  float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d, float scale,
                  int causal, fa_stream_t stream);
+
+/*
+ * Backward pass over unequal query/key lengths and padded batches, the
+ * gradient of fa_fwd_varlen for the same arguments.
+ *   q, dO, o    : [B][H][Nq][d] (q, dO bf16; o fp32);  lse : fp32 [B][H][Nq].
+ *   k, v        : bf16 [B][H][Nk][d].
+ *   dq          : fp32 [B][H][Nq][d];  dk, dv : fp32 [B][H][Nk][d], overwritten.
+ *   workspace   : fp32, fa_bwd_workspace_bytes(B, H, Nq) bytes, or NULL as
+ *                 for fa_bwd; it ends holding D for each query row.
+ *   seqlens_q, seqlens_k : as fa_fwd_varlen (NULL: every row valid).
+ * Alignment and masking follow fa_fwd_varlen.  Padding rows and rows with no
+ * eligible key get zero gradients (and D = 0); key rows past the valid length
+ * get dK = dV = 0.  Padding rows of q, k, v and dO do not affect the result
+ * under the same bound as fa_fwd_varlen.  fa_bwd(...) equals
+ * fa_bwd_varlen(..., NULL, NULL, B, H, N, N, ...).
+ */
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                        const void* dO, float* dq, float* dk, float* dv, float* workspace, const int* seqlens_q,
+                        const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                        fa_stream_t stream);
 
 /*
  * Largest B*H*N that fa_bwd_noalloc accepts: 2^20 rows, i.e. 4 MiB of fp32
@@ -150,7 +196,8 @@ fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, c
                        const void* dO, float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d,
                        float scale, int causal, fa_stream_t stream);
 
-/* Bytes of the fa_bwd workspace: B*H*N fp32 values (0 on invalid sizes). */
+/* Bytes of the fa_bwd workspace: B*H*N fp32 values (0 on invalid sizes);
+ * for fa_bwd_varlen pass N = Nq. */
 size_t fa_bwd_workspace_bytes(int B, int H, int N);
 
 /*

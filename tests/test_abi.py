@@ -94,6 +94,28 @@ def test_bwd_argument_errors(fa, args, expect):
     assert st == expect, fa.fa_status_string(st)
 
 
+@pytest.mark.parametrize("call", ["fwd", "bwd"])
+@pytest.mark.parametrize("args,expect", [
+    (dict(Nk=0), 1),
+    (dict(Nq=-1), 1),
+    (dict(sq=FAKE + 2), 3),
+    (dict(sk=FAKE + 1), 3),
+    (dict(k=FAKE + 8), 3),
+    (dict(d=80), 2),
+])
+def test_varlen_argument_errors(fa, call, args, expect):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, do=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, ws=FAKE, sq=FAKE, sk=FAKE,
+             B=2, H=2, Nq=1, Nk=300, d=128, scale=0.1, causal=1)
+    a.update(args)
+    if call == "fwd":
+        st = fa.fa_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["sq"], a["sk"], a["B"], a["H"], a["Nq"],
+                              a["Nk"], a["d"], a["scale"], a["causal"], 0)
+    else:
+        st = fa.fa_bwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"], a["ws"],
+                              a["sq"], a["sk"], a["B"], a["H"], a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"], 0)
+    assert st == expect, fa.fa_status_string(st)
+
+
 def test_status_strings(fa):
     seen = set()
     for code in range(7):

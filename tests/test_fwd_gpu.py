@@ -107,6 +107,25 @@ def test_masked_positions_do_not_leak():
     assert torch.equal(l1[:, :, :160], l2[:, :, :160])
 
 
+def test_key_order_and_tile_boundaries():
+    """Permuting the keys (with their values) regroups them into different
+    tiles and changes which tile holds each row's maximum, but not the
+    attention result: both orders match the oracle, and each other to the
+    rounding of P to bf16."""
+    inp = workloads.make_inputs(1, 2, 777, 128, seed=21)
+    scale = scale_for(128)
+    perm = torch.randperm(777, generator=torch.Generator().manual_seed(5))
+    shuffled = dict(inp)
+    shuffled["k"] = inp["k"][:, :, perm].contiguous()
+    shuffled["v"] = inp["v"][:, :, perm].contiguous()
+    o1, l1 = gpu_forward(inp, False, scale)
+    o2, l2 = gpu_forward(shuffled, False, scale)
+    o_ref, lse_ref = oracle.forward(to64(inp["q"]), to64(inp["k"]), to64(inp["v"]), scale, False)
+    assert_forward_close(o1.numpy(), l1.numpy(), o_ref, lse_ref, "original order")
+    assert_forward_close(o2.numpy(), l2.numpy(), o_ref, lse_ref, "permuted keys")
+    assert (o1 - o2).abs().max() <= 2e-3
+
+
 def test_head_result_independent_of_batch_position():
     """A head computed alone equals the same head inside a larger batch
     (different CTA and scheduling)."""
