@@ -10,6 +10,10 @@ workload: B=4, H=16, N=8192, d=128, causal, bf16 inputs ~ N(0,1).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--fwd-only]
 
+With ``--workload decode_b8_h32_nq1_nk32768_d128`` a step is one decoding
+step through fa_fwd_decode (one query row per head against a 32k-key cache)
+and the metric is the compulsory HBM traffic per second (K and V read once).
+
 Prints one JSON line on rank 0.  ``--impl reference`` times the fp64 CPU
 oracle (the only reference implementation there is) on a bounded sample of
 the same workload.  Under torchrun each rank runs its own batch (heads are
@@ -34,6 +38,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 and fraction of dense BF16 tensor peak"
+DECODE_METRIC = "attention decode step: compulsory HBM GB/s (K, V read once) on 1 GB300 and fraction of HBM peak"
 DEFAULT_WORKLOAD = "training_b4_h16_n8192_d128_causal"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 L2_BYTES = 126 * 1024 * 1024
@@ -65,10 +70,11 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
-    "fwd_kernel": ["fwd.cu", "ptx.cuh", "fa_sched.h", "internal.h"],
-    "preprocess_kernel": ["bwd.cu", "ptx.cuh", "fa_sched.h", "internal.h"],
-    "dq_kernel": ["bwd.cu", "ptx.cuh", "fa_sched.h", "internal.h"],
-    "dkdv_kernel": ["bwd.cu", "ptx.cuh", "fa_sched.h", "internal.h"],
+    "fwd_kernel": ["fwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
+    "preprocess_kernel": ["bwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
+    "dq_kernel": ["bwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
+    "dkdv_kernel": ["bwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
+    "decode_kernel": ["decode.cu", "geom.cuh", "ptx.cuh", "internal.h"],
 }
 
 
@@ -407,6 +413,133 @@ def run_ours(args):
     return line
 
 
+# ------------------------------------------------------------ decode arm
+
+def run_decode(args):
+    import torch
+    import exact_tiled_attention_18_gb300 as fa
+    from exact_tiled_attention_18_gb300 import workloads
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(rank, world, "nccl")
+    w = workloads.DECODE_WORKLOADS[args.workload]
+    peaks, peak_kind = load_peaks()
+    inp = workloads.make_decode_inputs(w.B, w.H, w.Nq, w.Nk, w.d, seed=rank)
+    q, k, v = (inp[n].to(device) for n in ("q", "k", "v"))
+    o = torch.empty((w.B, w.H, w.Nq, w.d), dtype=torch.float32, device=device)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=device)
+    ws = torch.empty(fa.fa_fwd_decode_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d) // 4, dtype=torch.float32,
+                     device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fa.forward_decode(q, k, v, causal=w.causal, scale=w.scale, workspace=ws, out=(o, lse))
+
+    for _ in range(args.warmup):
+        step()
+    fa.sync_status(device)
+    sampler = ClockSampler(local) if rank == 0 else None
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.start()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop() if sampler else None
+    barrier(dist, device)
+    fa.sync_status(device)
+    ms = max_over_ranks(a.elapsed_time(b), dist, device) / args.steps
+    gbs = w.hbm_bytes() * world / (ms * 1e-3) / 1e9
+
+    e2e = None
+    if args.e2e_steps > 0:
+        host_in = {n: inp[n].pin_memory() for n in ("q", "k", "v")}
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse)]
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def e2e_step():
+            qq, kk, vv = (host_in[n].to(device, non_blocking=True) for n in ("q", "k", "v"))
+            outs = fa.forward_decode(qq, kk, vv, causal=w.causal, scale=w.scale, workspace=ws)
+            for h, g in zip(host_out, outs):
+                h.copy_(g, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+        a.record(stream)
+        n_e2e = min(args.e2e_steps, 3)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        fa.sync_status(device)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), dist, device) / n_e2e
+        e2e = {"value": round(w.hbm_bytes() * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gb, heads, secs = decode_oracle_sample(w, 5.0)
+        cpu = {"value": round(gb, 4), "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"{heads} whole head(s) of the workload (Nq={w.Nq}, Nk={w.Nk}, d={w.d}), "
+                         f"numpy fp64 row by row, {secs:.1f} s"}
+    if rank != 0:
+        return None
+    hbm = peaks["hbm_gbs"]
+    return {
+        "metric": DECODE_METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+                   "step": "decode fwd",
+                   "l2": f"K,V {w.kv_bytes() / 2**30:.2f} GiB > L2; no flush",
+                   "parallelism": f"heads independent; {world} rank(s) x own batch, no collective"},
+        "tflops": round(w.flops() * world / (ms * 1e-3) / 1e12, 3),
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel + decode_combine_kernel (one C call, timed together)",
+                     "achieved": round(w.hbm_bytes() / (ms * 1e-3) / 1e9, 2), "peak": hbm, "unit": "GB/s",
+                     "frac": round(w.hbm_bytes() / (ms * 1e-3) / 1e9 / hbm, 4),
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth", "algorithmic_per_launch": w.hbm_bytes(),
+                     "ms_per_launch": round(ms, 4), "traffic": ncu_traffic("decode_kernel", w.name)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+
+
+def decode_oracle_sample(w, budget_s):
+    """Time the fp64 oracle on whole heads of a decode workload; returns
+    (GB/s of the workload's compulsory bytes, heads, seconds)."""
+    import oracle
+    from exact_tiled_attention_18_gb300 import workloads
+    inp = workloads.make_decode_inputs(1, 1, w.Nq, w.Nk, w.d, seed=0)
+    x = {n: inp[n].float().double().numpy() for n in inp}
+    heads, t_total = 0, 0.0
+    rows = [(0, 0, i) for i in range(w.Nq)]
+    while heads < w.B * w.H and (heads == 0 or t_total < budget_s):
+        t0 = time.perf_counter()
+        oracle.forward_rows(x["q"], x["k"], x["v"], w.scale, w.causal, rows)
+        t_total += time.perf_counter() - t0
+        heads += 1
+    return w.hbm_bytes() / (w.B * w.H) * heads / t_total / 1e9, heads, t_total
+
+
 # ----------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -415,6 +548,8 @@ def run_reference(args):
         return None
     from exact_tiled_attention_18_gb300 import workloads
     import oracle
+    if args.workload in workloads.DECODE_WORKLOADS:
+        return run_reference_decode(args)
     w = workloads.WORKLOADS[args.workload]
     do_bwd = w.backward and not args.fwd_only
     # each step: the fp64 oracle on a causal prefix of one head (the first
@@ -463,9 +598,49 @@ def run_reference(args):
     }
 
 
+def run_reference_decode(args):
+    """The fp64 oracle on whole heads of a decode workload, each step a
+    bounded sample (8 heads)."""
+    import oracle
+    from exact_tiled_attention_18_gb300 import workloads
+    w = workloads.DECODE_WORKLOADS[args.workload]
+    heads = 8
+    inp = workloads.make_decode_inputs(1, heads, w.Nq, w.Nk, w.d, seed=0)
+    x = {n: inp[n].float().double().numpy() for n in inp}
+    rows = [(0, h, i) for h in range(heads) for i in range(w.Nq)]
+
+    def step():
+        oracle.forward_rows(x["q"], x["k"], x["v"], w.scale, w.causal, rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    value = w.hbm_bytes() / (w.B * w.H) * heads / (ms * 1e-3) / 1e9
+    sample = f"fp64 numpy oracle on {heads} whole heads (Nq={w.Nq}, Nk={w.Nk}, d={w.d}) per step"
+    return {
+        "impl": "reference", "metric": DECODE_METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+                   "step": "decode fwd"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main(argv=None):
     args = parse_args(argv)
-    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    from exact_tiled_attention_18_gb300 import workloads
+    if args.impl == "reference":
+        line = run_reference(args)
+    elif args.workload in workloads.DECODE_WORKLOADS:
+        line = run_decode(args)
+    else:
+        line = run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -20,6 +20,7 @@ FA_ERR_MISALIGNED = 3
 FA_ERR_LAUNCH = 4
 FA_ERR_TIMEOUT = 5
 FA_ERR_DEVICE_FAULT = 6
+FA_DECODE_MAX_Q = 8
 
 _lock = threading.Lock()
 _lib = None
@@ -48,6 +49,10 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd.restype = st
         L.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_fwd_varlen.restype = st
+        L.fa_fwd_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_fwd_decode.restype = st
+        L.fa_fwd_decode_workspace_bytes.argtypes = [i, i, i, i, i]
+        L.fa_fwd_decode_workspace_bytes.restype = ctypes.c_size_t
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd.restype = st
         L.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
@@ -90,6 +95,16 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: 
 def fa_fwd_varlen(q: int, k: int, v: int, o: int, lse: int, seqlens_q: int, seqlens_k: int, B: int, H: int,
                   Nq: int, Nk: int, d: int, scale: float, causal: int, stream: int) -> int:
     return lib().fa_fwd_varlen(q, k, v, o, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream)
+
+
+def fa_fwd_decode(q: int, k: int, v: int, o: int, lse: int, seqlens_q: int, seqlens_k: int, workspace: int, B: int,
+                  H: int, Nq: int, Nk: int, d: int, scale: float, causal: int, stream: int) -> int:
+    return lib().fa_fwd_decode(q, k, v, o, lse, seqlens_q, seqlens_k, workspace, B, H, Nq, Nk, d, scale, causal,
+                               stream)
+
+
+def fa_fwd_decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return lib().fa_fwd_decode_workspace_bytes(B, H, Nq, Nk, d)
 
 
 def fa_bwd(q: int, k: int, v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int, workspace: int,
@@ -209,6 +224,36 @@ def forward_varlen(q, k, v, seqlens_q=None, seqlens_k=None, causal: bool = False
     _check("fa_fwd_varlen", fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                           seqlens_q.data_ptr() if seqlens_q is not None else 0,
                                           seqlens_k.data_ptr() if seqlens_k is not None else 0,
+                                          B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    return o, lse
+
+
+def forward_decode(q, k, v, seqlens_q=None, seqlens_k=None, causal: bool = False, scale: float | None = None,
+                   workspace=None, out=None):
+    """O, LSE through fa_fwd_decode: q [B,H,Nq,d] with Nq <= FA_DECODE_MAX_Q,
+    k and v [B,H,Nk,d] (bf16, CUDA); same results as forward_varlen."""
+    import torch
+    for t in (q, k, v):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v must be contiguous 4-D bf16 CUDA tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, H, Nk, d] with the batch, heads and d of q")
+    for t in (seqlens_q, seqlens_k):
+        if t is not None and (not t.is_cuda or t.dtype != torch.int32 or t.numel() != B or not t.is_contiguous()):
+            raise ValueError("seqlens must be contiguous int32 CUDA tensors of B entries")
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    if out is None:
+        o = torch.empty((B, H, Nq, d), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    _check("fa_fwd_decode", fa_fwd_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                          seqlens_q.data_ptr() if seqlens_q is not None else 0,
+                                          seqlens_k.data_ptr() if seqlens_k is not None else 0,
+                                          workspace.data_ptr() if workspace is not None else 0,
                                           B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
     return o, lse
 

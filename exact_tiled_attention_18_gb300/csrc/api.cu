@@ -65,12 +65,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 3-D view [heads][n][d] of a contiguous bf16 tensor; box = 64 columns x 128
 // rows x 1 head with 128-byte swizzle (the layout the MMA descriptors
 // expect).  Rows past n read as zeros.
-bool encode_bf16_map(CUtensorMap* m, const void* base, int heads, int n, int d) {
+bool encode_bf16_map(CUtensorMap* m, const void* base, int heads, int n, int d, int box_rows = fa::kTileRows) {
   auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(heads)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(n) * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -214,6 +214,27 @@ fa_status bwd_prepare(fa::BwdArgs& a, const void* q, const void* k, const void* 
   return FA_OK;
 }
 
+// Key splits of the decode kernel.  Each split is at least kDecodeMinChunk
+// keys; the count aims at a few waves of two resident CTAs per SM over all
+// heads, and is capped so that the workspace bound below holds.
+constexpr int kDecodeMinChunk = 512;
+constexpr int kDecodeMaxSplits = 256;
+
+int decode_max_splits(int Nk) {
+  const int s = (Nk + kDecodeMinChunk - 1) / kDecodeMinChunk;
+  return s < 1 ? 1 : (s > kDecodeMaxSplits ? kDecodeMaxSplits : s);
+}
+
+void decode_splits(int heads, int Nk, int sms, int& splits, int& chunk) {
+  const long long target = 4LL * 2 * sms;  // four waves of two CTAs per SM
+  long long s = (target + heads - 1) / heads;
+  const int cap = decode_max_splits(Nk);
+  if (s > cap) s = cap;
+  if (s < 1) s = 1;
+  chunk = static_cast<int>(((Nk + s - 1) / s + 63) / 64 * 64);
+  splits = (Nk + chunk - 1) / chunk;
+}
+
 }  // namespace
 
 extern "C" {
@@ -227,6 +248,62 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, f
                         const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                         fa_stream_t stream) {
   return fwd_common(q, k, v, o, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream);
+}
+
+size_t fa_fwd_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || Nq > FA_DECODE_MAX_Q || Nk < 1 || (d != 64 && d != 128)) return 0;
+  if (static_cast<long long>(B) * H * Nk >= (1LL << 31)) return 0;
+  return static_cast<size_t>(B) * H * decode_max_splits(Nk) * Nq * (d + 1) * sizeof(float);
+}
+
+fa_status fa_fwd_decode(const void* q, const void* k, const void* v, float* o, float* lse, const int* seqlens_q,
+                        const int* seqlens_k, float* workspace, int B, int H, int Nq, int Nk, int d, float scale,
+                        int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, Nk, d, causal);
+  if (st != FA_OK) return st;
+  if (Nq < 1 || Nq > FA_DECODE_MAX_Q) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      (workspace && !aligned(workspace, 16)) || (seqlens_q && !aligned(seqlens_q, 4)) ||
+      (seqlens_k && !aligned(seqlens_k, 4)))
+    return FA_ERR_MISALIGNED;
+  DeviceInfo di;
+  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
+  const int heads = B * H;
+  fa::DecArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_bf16_map(&a.tm_k, k, heads, Nk, d, 64) || !encode_bf16_map(&a.tm_v, v, heads, Nk, d, 64))
+    return FA_ERR_LAUNCH;
+  a.q = static_cast<const uint16_t*>(q);
+  a.o = o;
+  a.lse = lse;
+  a.geom.nq = Nq;
+  a.geom.nk = Nk;
+  a.geom.seqlens_q = seqlens_q;
+  a.geom.seqlens_k = seqlens_k;
+  a.geom.heads_per_batch = H;
+  a.heads = heads;
+  a.d = d;
+  a.causal = causal;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  decode_splits(heads, Nk, di.sms, a.splits, a.chunk);
+  a.status = di.status;
+  a.wait_limit_ns = wait_limit_ns();
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* part = workspace;
+  if (a.splits > 1 && !part) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&part), fa_fwd_decode_workspace_bytes(B, H, Nq, Nk, d), s) !=
+        cudaSuccess)
+      return FA_ERR_LAUNCH;
+  }
+  a.part = part;
+  cudaError_t e = fa::launch_decode(a, s);
+  if (part && !workspace) {
+    cudaError_t e2 = cudaFreeAsync(part, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int N) {

@@ -87,14 +87,26 @@ struct FwdLayout {
 
 // Valid lengths and key-tile counts of one work unit (a head and its query
 // tiles 2*pair and 2*pair+1); a count of 0 means the tile has nothing to
-// compute (all padding, or no eligible key).
+// compute (all padding, or no eligible key).  VARLEN = false is the square
+// call (Nq = Nk, no per-sequence lengths): offset 0, no padding rows, and tile
+// 2*pair never has more key tiles than 2*pair+1 nor none at all, facts the
+// compiler folds into the loops below.
 struct UnitGeom {
   int lq, lk, off, nkt, na, nb;
 };
 
+template <bool VARLEN>
 __device__ __forceinline__ UnitGeom unit_geom(const SeqGeom& g, int head, int pair, bool causal) {
-  const HeadLen h = head_len(g, head);
   UnitGeom u;
+  if constexpr (!VARLEN) {
+    u.lq = u.lk = g.nq;
+    u.off = 0;
+    u.nkt = (g.nq + kTileRows - 1) / kTileRows;
+    u.na = causal ? min(2 * pair + 1, u.nkt) : u.nkt;
+    u.nb = causal ? min(2 * pair + 2, u.nkt) : u.nkt;
+    return u;
+  }
+  const HeadLen h = head_len(g, head);
   u.lq = h.lq;
   u.lk = h.lk;
   u.off = h.off;
@@ -121,7 +133,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, float* __restrict__ o, float* __restrict__ lse,
@@ -185,13 +197,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     int head, pair;
     bool ok = true;
     while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
-      const UnitGeom u = unit_geom(geom, head, pair, CAUSAL);
+      const UnitGeom u = unit_geom<VARLEN>(geom, head, pair, CAUSAL);
       const int nt = t ? u.nb : u.na;
       const int qtile = 2 * pair + t;
       const int row = qtile * kTileRows + r;
       const int unit = head * sp.units_per_head + pair;
       float m_ref = 0.f, l = 0.f;
-      if (nt == 0) {
+      if (VARLEN && nt == 0) {
         // no key for any row of this tile (or all padding): O = 0, LSE = -inf
         if (row < nq) {
           float* orow = o + (static_cast<size_t>(head) * nq + row) * D;
@@ -218,7 +230,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // warp's rescale vote and its values cannot change valid rows' rounding
         const bool diag = CAUSAL && (j * kTileRows + kTileRows - 1 > qtile * kTileRows + u.off);
         const bool tail = (j == u.nkt - 1) && ((u.lk & (kTileRows - 1)) != 0);
-        const bool padq = qtile * kTileRows + kTileRows > u.lq;
+        const bool padq = VARLEN && qtile * kTileRows + kTileRows > u.lq;
         if (diag || tail || padq) {
           const int lim = row < u.lq ? (CAUSAL ? min(row + u.off + 1, u.lk) : u.lk) - j * kTileRows : 0;
 #pragma unroll
@@ -298,7 +310,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // rows past the valid length are padding and rows without an eligible
       // key have l = 0: both get O = 0, LSE = -inf (selected, so that what a
       // padding row accumulated never reaches the output)
-      const bool live = l > 0.f && row < u.lq;
+      const bool live = l > 0.f && (!VARLEN || row < u.lq);
       const float inv = live ? 1.0f / l : 0.f;
       const bool valid = row < nq;
       float* orow = o + (static_cast<size_t>(head) * nq + row) * D;
@@ -307,7 +319,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         uint32_t v[32];
         tmem_ld32(tO + 32 * c, v);
         tmem_ld_wait();
-        if (!live) {
+        if (VARLEN && !live) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
@@ -339,9 +351,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int head, pair;
       bool ok = true;
       while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
-        const UnitGeom u = unit_geom(geom, head, pair, CAUSAL);
-        const int nmax = max(u.na, u.nb);
-        if (nmax == 0) continue;  // nothing to compute for this unit
+        const UnitGeom u = unit_geom<VARLEN>(geom, head, pair, CAUSAL);
+        const int nmax = VARLEN ? max(u.na, u.nb) : u.nb;
+        if (VARLEN && nmax == 0) continue;  // nothing to compute for this unit
         const int unit = head * sp.units_per_head + pair;
         ok = wait_bounded(BAR(L::Q_EMPTY), (qn & 1) ^ 1, wc, SITE_LOAD_Q, unit);
         if (!ok) break;
@@ -415,9 +427,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int head, pair;
       bool ok = true;
       while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
-        const UnitGeom u = unit_geom(geom, head, pair, CAUSAL);
-        const int na = u.na, nb = u.nb, nmax = max(na, nb);
-        if (nmax == 0) continue;  // nothing to compute for this unit
+        const UnitGeom u = unit_geom<VARLEN>(geom, head, pair, CAUSAL);
+        const int na = u.na, nb = u.nb, nmax = VARLEN ? max(na, nb) : nb;
+        if (VARLEN && nmax == 0) continue;  // nothing to compute for this unit
         const int unit = head * sp.units_per_head + pair;
         ok = wait_bounded(BAR(L::Q_FULL), qn & 1, wc, SITE_MMA_Q, unit);
         if (!ok) break;
@@ -425,19 +437,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ok = wait_bounded(BAR(L::KV_FULL + kvbase % S), (kvbase / S) & 1, wc, SITE_MMA_KV, unit);
         if (!ok) break;
         tc_fence_after();
-        if (na > 0) {
+        if (!VARLEN || na > 0) {
           issue_s(0, slot_addr(kvbase));
           umma_commit(BAR(L::S_FULL + 0));
         }
-        if (nb > 0) {
+        if (!VARLEN || nb > 0) {
           issue_s(1, slot_addr(kvbase));
           umma_commit(BAR(L::S_FULL + 1));
         }
         for (int j = 0; j < nmax; ++j) {
           const uint32_t kpos = kvbase + 2 * j, vpos = kpos + 1, knext = kpos + 2;
-          const bool has_a = j < na, next_a = j + 1 < na, has_b = j < nb, next_b = j + 1 < nb;
+          const bool has_a = j < na, next_a = j + 1 < na, has_b = !VARLEN || j < nb, next_b = j + 1 < nb;
           umma_commit(BAR(L::KV_EMPTY + kpos % S));  // K_j is free once S(j) of both tiles completes
-          if (!next_a && !next_b) umma_commit(BAR(L::Q_EMPTY));  // the unit's last S has been issued
+          if (!next_b && (!VARLEN || !next_a)) umma_commit(BAR(L::Q_EMPTY));  // the unit's last S has been issued
           ok = wait_bounded(BAR(L::KV_FULL + vpos % S), (vpos / S) & 1, wc, SITE_MMA_KV, unit);
           if (!ok) break;
           if (has_a) {
@@ -490,10 +502,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
-cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+template <int D, bool CAUSAL, bool VARLEN>
+cudaError_t launch_fwd_v(const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto kern = fwd_kernel<D, CAUSAL>;
+  auto kern = fwd_kernel<D, CAUSAL, VARLEN>;
   cudaFuncAttributes fattr;
   cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
   if (e != cudaSuccess) return e;
@@ -505,6 +517,12 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
                                                              a.scale_log2, a.sched, a.status, a.wait_limit_ns,
                                                              a.stall_unit);
   return cudaGetLastError();
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  const bool square = !a.geom.seqlens_q && !a.geom.seqlens_k && a.geom.nq == a.geom.nk;
+  return square ? launch_fwd_v<D, CAUSAL, false>(a, stream) : launch_fwd_v<D, CAUSAL, true>(a, stream);
 }
 
 }  // namespace

@@ -61,6 +61,25 @@ struct BwdArgs {
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 
+struct DecArgs {
+  CUtensorMap tm_k, tm_v;  // 3-D maps over [B*H][Nk][d] bf16, box 64 x 64 x 1, 128-byte swizzle
+  const uint16_t* q;       // [B*H][Nq][d] bf16
+  float* o;                // [B*H][Nq][d] fp32
+  float* lse;              // [B*H][Nq] fp32
+  float* part;             // splits > 1: [B*H][splits][Nq][d] outputs, then [B*H][splits][Nq] log2-sum-exp
+  SeqGeom geom;
+  int heads;
+  int d;
+  int causal;
+  float scale_log2;
+  int splits;              // key splits per head (one CTA each)
+  int chunk;               // keys per split, a multiple of 64
+  int* status;
+  unsigned long long wait_limit_ns;
+};
+
+cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);
+
 // The three stages of launch_bwd, for callers that time or order them
 // separately: 0 = preprocess (D'), 1 = dQ (corrects D), 2 = dK/dV.
 cudaError_t launch_bwd_stage(const BwdArgs& a, int stage, cudaStream_t stream);

@@ -66,6 +66,56 @@ def randn_bf16(shape, seed: int) -> torch.Tensor:
     return torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
 
 
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """One decoding step: Nq query rows per head against Nk cached keys and
+    values (causal, aligned at the last key)."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool = True
+
+    @property
+    def scale(self) -> float:
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32))
+
+    def kv_bytes(self) -> int:
+        """K and V read once: the compulsory HBM traffic that bounds the step."""
+        return 2 * self.B * self.H * self.Nk * self.d * 2
+
+    def hbm_bytes(self) -> int:
+        """K, V and q read (bf16), O (fp32) and LSE (fp32) written."""
+        rows = self.B * self.H * self.Nq
+        return self.kv_bytes() + rows * self.d * 2 + rows * self.d * 4 + rows * 4
+
+    def flops(self) -> float:
+        """4*d FLOPs per (query, eligible key) pair."""
+        pairs = sum(min(i + 1 + self.Nk - self.Nq, self.Nk) if self.causal else self.Nk for i in range(self.Nq))
+        return 4.0 * self.B * self.H * pairs * self.d
+
+
+# A decoding step of 8 sequences x 32 heads over a 32k-token cache: K and V
+# are 4.3 GB, far larger than L2, and are read once.
+DECODE_WORKLOADS = {
+    "decode_b8_h32_nq1_nk32768_d128": DecodeWorkload("decode_b8_h32_nq1_nk32768_d128", 8, 32, 1, 32768, 128),
+}
+
+
+def make_decode_inputs(B: int, H: int, Nq: int, Nk: int, d: int, seed: int = 0) -> dict:
+    """CPU bf16 q [B, H, Nq, d] and k, v [B, H, Nk, d], successive N(0, 1)
+    draws of one seeded generator."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    out = {}
+    for name, n in (("q", Nq), ("k", Nk), ("v", Nk)):
+        out[name] = torch.randn(B, H, n, d, generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return out
+
+
 def make_inputs(B: int, H: int, N: int, d: int, seed: int = 0, with_grad: bool = False,
                 boost_every: int = 0, boost: float = 1.0) -> dict:
     """Return CPU bf16 tensors q, k, v (and dO) of shape [B, H, N, d].

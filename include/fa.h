@@ -110,6 +110,36 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, f
                         const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                         fa_stream_t stream);
 
+/* Most query rows per head that fa_fwd_decode accepts. */
+#define FA_DECODE_MAX_Q 8
+
+/*
+ * Decode-shaped forward: 1 <= Nq <= FA_DECODE_MAX_Q query rows per head
+ * against a long key/value history.  Computes exactly what fa_fwd_varlen
+ * computes for the same arguments (same layouts, lengths, bottom-right causal
+ * alignment, padding rules and outputs), with a kernel built for this shape:
+ * single-token decoding reads all of K and V once per step for one query row,
+ * about one FLOP per byte, so it is bound by HBM bandwidth rather than by the
+ * tensor cores ("FlashAttention Interview Questions ...", final section, on
+ * prefill against single-token decoding).  Each head's keys are split over
+ * many CTAs that stream K/V once; a second kernel merges the splits by their
+ * log-sum-exp.
+ *   workspace : fp32 scratch for the per-split results,
+ *               fa_fwd_decode_workspace_bytes(B, H, Nq, Nk, d) bytes,
+ *               16-byte aligned; or NULL, in which case the library takes a
+ *               stream-ordered allocation when it splits the keys and frees
+ *               it on the same stream.
+ * Errors as fa_fwd_varlen; Nq outside [1, FA_DECODE_MAX_Q] returns
+ * FA_ERR_INVALID_ARG.
+ */
+fa_status fa_fwd_decode(const void* q, const void* k, const void* v, float* o, float* lse, const int* seqlens_q,
+                        const int* seqlens_k, float* workspace, int B, int H, int Nq, int Nk, int d, float scale,
+                        int causal, fa_stream_t stream);
+
+/* Bytes of the fa_fwd_decode workspace (an upper bound that does not depend
+ * on the device); 0 on invalid sizes. */
+size_t fa_fwd_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+
 /*
  * Backward pass by recomputation: attention probabilities are rebuilt from
  * q, k and the saved lse instead of being stored ("FlashAttention Interview
