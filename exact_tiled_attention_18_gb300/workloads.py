@@ -102,6 +102,9 @@ class DecodeWorkload:
 # are 4.3 GB, far larger than L2, and are read once.
 DECODE_WORKLOADS = {
     "decode_b8_h32_nq1_nk32768_d128": DecodeWorkload("decode_b8_h32_nq1_nk32768_d128", 8, 32, 1, 32768, 128),
+    # a quarter of the batch (1.07 GB of K/V, still far larger than L2): the
+    # size on which multi-pass profiler captures are taken
+    "decode_b2_h32_nq1_nk32768_d128": DecodeWorkload("decode_b2_h32_nq1_nk32768_d128", 2, 32, 1, 32768, 128),
 }
 
 
