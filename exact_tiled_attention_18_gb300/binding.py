@@ -21,6 +21,8 @@ FA_ERR_LAUNCH = 4
 FA_ERR_TIMEOUT = 5
 FA_ERR_DEVICE_FAULT = 6
 FA_DECODE_MAX_Q = 8
+FA_DTYPE_F32 = 0
+FA_DTYPE_BF16 = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -49,6 +51,10 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd.restype = st
         L.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_fwd_varlen.restype = st
+        L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_fwd_ex.restype = st
+        L.fa_bwd_ex.argtypes = [vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_bwd_ex.restype = st
         L.fa_fwd_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_fwd_decode.restype = st
         L.fa_fwd_decode_workspace_bytes.argtypes = [i, i, i, i, i]
@@ -95,6 +101,18 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, d: 
 def fa_fwd_varlen(q: int, k: int, v: int, o: int, lse: int, seqlens_q: int, seqlens_k: int, B: int, H: int,
                   Nq: int, Nk: int, d: int, scale: float, causal: int, stream: int) -> int:
     return lib().fa_fwd_varlen(q, k, v, o, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream)
+
+
+def fa_fwd_ex(q: int, k: int, v: int, o: int, o_dtype: int, lse: int, seqlens_q: int, seqlens_k: int, B: int,
+              H: int, Nq: int, Nk: int, d: int, scale: float, causal: int, stream: int) -> int:
+    return lib().fa_fwd_ex(q, k, v, o, o_dtype, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream)
+
+
+def fa_bwd_ex(q: int, k: int, v: int, o: int, o_dtype: int, lse: int, do: int, dq: int, dk: int, dv: int,
+              workspace: int, seqlens_q: int, seqlens_k: int, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
+              causal: int, stream: int) -> int:
+    return lib().fa_bwd_ex(q, k, v, o, o_dtype, lse, do, dq, dk, dv, workspace, seqlens_q, seqlens_k, B, H, Nq, Nk,
+                           d, scale, causal, stream)
 
 
 def fa_fwd_decode(q: int, k: int, v: int, o: int, lse: int, seqlens_q: int, seqlens_k: int, workspace: int, B: int,
@@ -199,10 +217,11 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None)
 
 
 def forward_varlen(q, k, v, seqlens_q=None, seqlens_k=None, causal: bool = False, scale: float | None = None,
-                   out=None):
+                   out=None, o_dtype=None):
     """O, LSE through fa_fwd_varlen: q [B,H,Nq,d], k and v [B,H,Nk,d] (bf16,
     CUDA); seqlens_q / seqlens_k optional int32 CUDA tensors of B valid
-    lengths.  Causal alignment is bottom-right (see include/fa.h)."""
+    lengths.  Causal alignment is bottom-right (see include/fa.h).  With
+    o_dtype=torch.bfloat16 O is written as bf16 through fa_fwd_ex."""
     import torch
     for t in (q, k, v):
         if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
@@ -217,14 +236,22 @@ def forward_varlen(q, k, v, seqlens_q=None, seqlens_k=None, causal: bool = False
     if scale is None:
         scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
     if out is None:
-        o = torch.empty((B, H, Nq, d), dtype=torch.float32, device=q.device)
+        o = torch.empty((B, H, Nq, d), dtype=o_dtype or torch.float32, device=q.device)
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     else:
         o, lse = out
-    _check("fa_fwd_varlen", fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                          seqlens_q.data_ptr() if seqlens_q is not None else 0,
-                                          seqlens_k.data_ptr() if seqlens_k is not None else 0,
-                                          B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    sq = seqlens_q.data_ptr() if seqlens_q is not None else 0
+    sk = seqlens_k.data_ptr() if seqlens_k is not None else 0
+    if o.dtype == torch.float32:
+        _check("fa_fwd_varlen", fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                              sq, sk, B, H, Nq, Nk, d, scale, int(bool(causal)),
+                                              _stream_handle(q.device)))
+    elif o.dtype == torch.bfloat16:
+        _check("fa_fwd_ex", fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), FA_DTYPE_BF16,
+                                      lse.data_ptr(), sq, sk, B, H, Nq, Nk, d, scale, int(bool(causal)),
+                                      _stream_handle(q.device)))
+    else:
+        raise ValueError("O must be float32 or bfloat16")
     return o, lse
 
 
@@ -300,12 +327,15 @@ def backward_varlen(q, k, v, o, lse, do, seqlens_q=None, seqlens_k=None, causal:
     else:
         dq, dk, dv = out
     ws = workspace.data_ptr() if workspace is not None else 0
-    _check("fa_bwd_varlen",
-           fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
-                         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws,
-                         seqlens_q.data_ptr() if seqlens_q is not None else 0,
-                         seqlens_k.data_ptr() if seqlens_k is not None else 0,
-                         B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    if o.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("O must be float32 or bfloat16")
+    o_dtype = FA_DTYPE_BF16 if o.dtype == torch.bfloat16 else FA_DTYPE_F32
+    _check("fa_bwd_ex",
+           fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o_dtype, lse.data_ptr(), do.data_ptr(),
+                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws,
+                     seqlens_q.data_ptr() if seqlens_q is not None else 0,
+                     seqlens_k.data_ptr() if seqlens_k is not None else 0,
+                     B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
     return dq, dk, dv
 
 

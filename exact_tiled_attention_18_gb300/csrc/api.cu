@@ -123,10 +123,11 @@ fa::SchedParams make_sched(int heads, int n, int d, int causal, int grid_cap, lo
   return sp;
 }
 
-fa_status fwd_common(const void* q, const void* k, const void* v, float* o, float* lse, const int* seqlens_q,
-                     const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
-                     fa_stream_t stream) {
+fa_status fwd_common(const void* q, const void* k, const void* v, void* o, int o_dtype, float* lse,
+                     const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
+                     int causal, fa_stream_t stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (o_dtype != FA_DTYPE_F32 && o_dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   fa_status st = check_sizes(B, H, Nq, d, causal);
   if (st != FA_OK) return st;
   st = check_sizes(B, H, Nk, d, causal);
@@ -144,6 +145,7 @@ fa_status fwd_common(const void* q, const void* k, const void* v, float* o, floa
       !encode_bf16_map(&a.tm_v, v, heads, Nk, d))
     return FA_ERR_LAUNCH;
   a.o = o;
+  a.o_bf16 = o_dtype == FA_DTYPE_BF16;
   a.lse = lse;
   a.geom.nq = Nq;
   a.geom.nk = Nk;
@@ -163,11 +165,12 @@ fa_status fwd_common(const void* q, const void* k, const void* v, float* o, floa
 // Checks the arguments of a backward call (the workspace only for alignment;
 // it may be null) and fills every field of `a` but the row-term buffer.  q, dO, o, lse, dq: [B*H][Nq] rows; k, v, dk, dv:
 // [B*H][Nk] rows.
-fa_status bwd_prepare(fa::BwdArgs& a, const void* q, const void* k, const void* v, const float* o,
+fa_status bwd_prepare(fa::BwdArgs& a, const void* q, const void* k, const void* v, const void* o, int o_dtype,
                       const float* lse, const void* dO, float* dq, float* dk, float* dv, const float* workspace,
                       const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
                       int causal) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (o_dtype != FA_DTYPE_F32 && o_dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   fa_status st = check_sizes(B, H, Nq, d, causal);
   if (st != FA_OK) return st;
   st = check_sizes(B, H, Nk, d, causal);
@@ -186,6 +189,7 @@ fa_status bwd_prepare(fa::BwdArgs& a, const void* q, const void* k, const void* 
       !encode_bf16_map(&a.tm_v, v, heads, Nk, d) || !encode_bf16_map(&a.tm_do, dO, heads, Nq, d))
     return FA_ERR_LAUNCH;
   a.o = o;
+  a.o_bf16 = o_dtype == FA_DTYPE_BF16;
   a.lse = lse;
   a.dout = static_cast<const uint16_t*>(dO);
   a.dq = dq;
@@ -241,13 +245,19 @@ extern "C" {
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H, int N, int d,
                  float scale, int causal, fa_stream_t stream) {
-  return fwd_common(q, k, v, o, lse, nullptr, nullptr, B, H, N, N, d, scale, causal, stream);
+  return fwd_common(q, k, v, o, FA_DTYPE_F32, lse, nullptr, nullptr, B, H, N, N, d, scale, causal, stream);
 }
 
 fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, float* lse, const int* seqlens_q,
                         const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                         fa_stream_t stream) {
-  return fwd_common(q, k, v, o, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream);
+  return fwd_common(q, k, v, o, FA_DTYPE_F32, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream);
+}
+
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int o_dtype, float* lse,
+                    const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
+                    int causal, fa_stream_t stream) {
+  return fwd_common(q, k, v, o, o_dtype, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream);
 }
 
 size_t fa_fwd_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
@@ -312,13 +322,13 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N) {
   return static_cast<size_t>(B) * H * N * sizeof(float);
 }
 
-fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const float* o, const float* lse,
-                        const void* dO, float* dq, float* dk, float* dv, float* workspace, const int* seqlens_q,
-                        const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
-                        fa_stream_t stream) {
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, int o_dtype, const float* lse,
+                    const void* dO, float* dq, float* dk, float* dv, float* workspace, const int* seqlens_q,
+                    const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                    fa_stream_t stream) {
   fa::BwdArgs a;
-  fa_status st =
-      bwd_prepare(a, q, k, v, o, lse, dO, dq, dk, dv, workspace, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal);
+  fa_status st = bwd_prepare(a, q, k, v, o, o_dtype, lse, dO, dq, dk, dv, workspace, seqlens_q, seqlens_k, B, H, Nq,
+                             Nk, d, scale, causal);
   if (st != FA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float* delta = workspace;
@@ -335,11 +345,19 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const float
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                        const void* dO, float* dq, float* dk, float* dv, float* workspace, const int* seqlens_q,
+                        const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                        fa_stream_t stream) {
+  return fa_bwd_ex(q, k, v, o, FA_DTYPE_F32, lse, dO, dq, dk, dv, workspace, seqlens_q, seqlens_k, B, H, Nq, Nk, d,
+                   scale, causal, stream);
+}
+
 fa_status fa_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse, const void* dO,
                  float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d, float scale,
                  int causal, fa_stream_t stream) {
-  return fa_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, workspace, nullptr, nullptr, B, H, N, N, d, scale, causal,
-                       stream);
+  return fa_bwd_ex(q, k, v, o, FA_DTYPE_F32, lse, dO, dq, dk, dv, workspace, nullptr, nullptr, B, H, N, N, d, scale,
+                   causal, stream);
 }
 
 // Scratch of fa_bwd_noalloc: the backward row term D for up to
@@ -357,7 +375,8 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const floa
                          int causal, fa_stream_t stream) {
   fa::BwdArgs a;
   fa_status st =
-      bwd_prepare(a, q, k, v, o, lse, dO, dq, dk, dv, nullptr, nullptr, nullptr, B, H, N, N, d, scale, causal);
+      bwd_prepare(a, q, k, v, o, FA_DTYPE_F32, lse, dO, dq, dk, dv, nullptr, nullptr, nullptr, B, H, N, N, d, scale,
+                  causal);
   if (st != FA_OK) return st;
   if (static_cast<long long>(B) * H * N > FA_NOALLOC_MAX_ROWS) return FA_ERR_INVALID_ARG;
   int dev = -1;
@@ -380,7 +399,8 @@ fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, c
   if (stage < 0 || stage > 2 || !workspace) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a;
   fa_status st =
-      bwd_prepare(a, q, k, v, o, lse, dO, dq, dk, dv, workspace, nullptr, nullptr, B, H, N, N, d, scale, causal);
+      bwd_prepare(a, q, k, v, o, FA_DTYPE_F32, lse, dO, dq, dk, dv, workspace, nullptr, nullptr, B, H, N, N, d, scale,
+                  causal);
   if (st != FA_OK) return st;
   a.delta = workspace;
   return fa::launch_bwd_stage(a, stage, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK

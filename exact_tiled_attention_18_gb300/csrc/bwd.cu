@@ -92,8 +92,9 @@ __device__ __forceinline__ uint64_t f2_from(uint32_t a, uint32_t b) {
 // ------------------------------------------------------------------ preprocess
 // D_i = sum_c dO_ic O_ic.  d/8 threads per row, 8 elements per thread; the
 // loop bound is uniform across a warp so every lane reaches the shuffles.
-template <int D>
-__global__ void __launch_bounds__(256) preprocess_kernel(const float* __restrict__ o,
+// O is fp32, or bf16 when OBF16.
+template <int D, bool OBF16>
+__global__ void __launch_bounds__(256) preprocess_kernel(const void* __restrict__ o_,
                                                          const uint16_t* __restrict__ dout,
                                                          float* __restrict__ delta, const int rows) {
   constexpr int G = D / 8;            // threads per row
@@ -106,10 +107,21 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const float* __restrict
     const int row = base + gi;
     float acc = 0.f;
     if (row < rows) {
-      const float4* op = reinterpret_cast<const float4*>(o + static_cast<size_t>(row) * D) + 2 * sub;
       const uint4 h = __ldg(reinterpret_cast<const uint4*>(dout + static_cast<size_t>(row) * D) + sub);
-      const float4 a = __ldg(op);
-      const float4 b = __ldg(op + 1);
+      float4 a, b;
+      if constexpr (OBF16) {
+        const uint4 oh =
+            __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o_) + static_cast<size_t>(row) * D) + sub);
+        a = make_float4(bf16_bits_to_float(oh.x & 0xFFFFu), bf16_bits_to_float(oh.x >> 16),
+                        bf16_bits_to_float(oh.y & 0xFFFFu), bf16_bits_to_float(oh.y >> 16));
+        b = make_float4(bf16_bits_to_float(oh.z & 0xFFFFu), bf16_bits_to_float(oh.z >> 16),
+                        bf16_bits_to_float(oh.w & 0xFFFFu), bf16_bits_to_float(oh.w >> 16));
+      } else {
+        const float4* op =
+            reinterpret_cast<const float4*>(static_cast<const float*>(o_) + static_cast<size_t>(row) * D) + 2 * sub;
+        a = __ldg(op);
+        b = __ldg(op + 1);
+      }
       acc = a.x * bf16_bits_to_float(h.x & 0xFFFFu) + a.y * bf16_bits_to_float(h.x >> 16) +
             a.z * bf16_bits_to_float(h.y & 0xFFFFu) + a.w * bf16_bits_to_float(h.y >> 16) +
             b.x * bf16_bits_to_float(h.z & 0xFFFFu) + b.y * bf16_bits_to_float(h.z >> 16) +
@@ -897,7 +909,10 @@ template <int D, bool CAUSAL>
 cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
   if (stage == 0) {
-    preprocess_kernel<D><<<a.grid_pre, 256, 0, stream>>>(a.o, a.dout, a.delta, a.heads * a.geom.nq);
+    if (a.o_bf16)
+      preprocess_kernel<D, true><<<a.grid_pre, 256, 0, stream>>>(a.o, a.dout, a.delta, a.heads * a.geom.nq);
+    else
+      preprocess_kernel<D, false><<<a.grid_pre, 256, 0, stream>>>(a.o, a.dout, a.delta, a.heads * a.geom.nq);
   } else if (stage == 1) {
     // dQ first: it turns D' = rowsum(dO o O) into the exact row term
     using L = QLayout<D>;

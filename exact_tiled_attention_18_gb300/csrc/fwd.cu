@@ -136,9 +136,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
 template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, float* __restrict__ o, float* __restrict__ lse,
-               const SeqGeom geom, const float scale_log2, const SchedParams sp, int* status,
-               const unsigned long long limit_ns, const int stall_unit) {
+               const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o, float* __restrict__ lse,
+               const int o_bf16, const SeqGeom geom, const float scale_log2, const SchedParams sp,
+               int* status, const unsigned long long limit_ns, const int stall_unit) {
   using L = FwdLayout<D>;
   constexpr int S = L::kSlots;
   extern __shared__ uint8_t smem_raw[];
@@ -206,9 +206,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (VARLEN && nt == 0) {
         // no key for any row of this tile (or all padding): O = 0, LSE = -inf
         if (row < nq) {
-          float* orow = o + (static_cast<size_t>(head) * nq + row) * D;
+          // D fp32 or D bf16 zeros: 4 D or 2 D bytes, in 16-byte stores
+          uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(o) +
+                                                 (static_cast<size_t>(head) * nq + row) * D * (o_bf16 ? 2 : 4));
 #pragma unroll 1
-          for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c = 0; c < (o_bf16 ? D / 8 : D / 4); ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
           lse[static_cast<size_t>(head) * nq + row] = -CUDART_INF_F;
         }
         continue;
@@ -313,7 +315,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const bool live = l > 0.f && (!VARLEN || row < u.lq);
       const float inv = live ? 1.0f / l : 0.f;
       const bool valid = row < nq;
-      float* orow = o + (static_cast<size_t>(head) * nq + row) * D;
+      float* orow = static_cast<float*>(o) + (static_cast<size_t>(head) * nq + row) * D;
+      uint16_t* orow_h = static_cast<uint16_t*>(o) + (static_cast<size_t>(head) * nq + row) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
@@ -323,7 +326,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        if (valid) {
+        if (valid && o_bf16) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 h;
+            h.x = pack_bf16x2(__uint_as_float(v[8 * i + 0]) * inv, __uint_as_float(v[8 * i + 1]) * inv);
+            h.y = pack_bf16x2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv);
+            h.z = pack_bf16x2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv);
+            h.w = pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow_h + 32 * c + 8 * i) = h;
+          }
+        } else if (valid) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float4 w;
@@ -513,7 +526,7 @@ cudaError_t launch_fwd_v(const FwdArgs& a, cudaStream_t stream) {
   if (fattr.numRegs != kFwdLaunchRegs) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
   if (e != cudaSuccess) return e;
-  kern<<<a.sched.grid, kFwdThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.geom,
+  kern<<<a.sched.grid, kFwdThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.o_bf16, a.geom,
                                                              a.scale_log2, a.sched, a.status, a.wait_limit_ns,
                                                              a.stall_unit);
   return cudaGetLastError();

@@ -21,8 +21,9 @@ struct SeqGeom {
 
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v;  // 3-D maps over [B*H][Nq or Nk][d] bf16, box 64 x 128 x 1, 128-byte swizzle
-  float* o;                      // [B*H][Nq][d] fp32
+  void* o;                       // [B*H][Nq][d] fp32, or bf16 when o_bf16
   float* lse;                    // [B*H][Nq] fp32
+  int o_bf16;
   SeqGeom geom;
   int d;                         // head dimension (64 or 128)
   int causal;
@@ -37,7 +38,8 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 maps as for the forward pass
-  const float* o;                       // forward output, fp32
+  const void* o;                        // forward output, fp32 (or bf16 when o_bf16)
+  int o_bf16;
   const float* lse;                     // forward log-sum-exp, fp32
   const uint16_t* dout;                 // dO, bf16 bits
   float* dq;

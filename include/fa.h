@@ -68,6 +68,12 @@ typedef enum {
   FA_ERR_DEVICE_FAULT = 6   /* the stream reported a CUDA error while synchronising */
 } fa_status;
 
+/* Element type of the forward output O (fa_fwd_ex, fa_bwd_ex). */
+typedef enum {
+  FA_DTYPE_F32 = 0,  /* fp32 O */
+  FA_DTYPE_BF16 = 1  /* bf16 O: the fp32 result rounded to nearest even, half the bytes written */
+} fa_dtype;
+
 /*
  * Forward pass.
  *   q, k, v : bf16 [B][H][N][d], read only.
@@ -112,6 +118,20 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, f
 
 /* Most query rows per head that fa_fwd_decode accepts. */
 #define FA_DECODE_MAX_Q 8
+
+/*
+ * The general forward: fa_fwd_varlen with a choice of output type.
+ *   o       : [B][H][Nq][d] of o_dtype (FA_DTYPE_F32 or FA_DTYPE_BF16),
+ *             16-byte aligned.  With FA_DTYPE_BF16 each element is the fp32
+ *             result of fa_fwd_varlen rounded to the nearest bf16 (ties to
+ *             even); LSE stays fp32.
+ * Other arguments, results and errors as fa_fwd_varlen; an o_dtype outside
+ * the enum returns FA_ERR_INVALID_ARG.  fa_fwd_varlen(...) equals
+ * fa_fwd_ex(..., FA_DTYPE_F32, ...).
+ */
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int o_dtype, float* lse,
+                    const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
+                    int causal, fa_stream_t stream);
 
 /*
  * Decode-shaped forward: 1 <= Nq <= FA_DECODE_MAX_Q query rows per head
@@ -179,6 +199,19 @@ fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const float
                         const void* dO, float* dq, float* dk, float* dv, float* workspace, const int* seqlens_q,
                         const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                         fa_stream_t stream);
+
+/*
+ * The general backward: fa_bwd_varlen taking O of either output type of
+ * fa_fwd_ex (o_dtype as there).  O only enters through the row term
+ * D_i = sum_c dO_ic O_ic, which the dQ stage corrects to the exact
+ * sum_j P_ij dP_ij of the recomputed probabilities, so a bf16 O leaves the
+ * gradients' accuracy unchanged.  fa_bwd_varlen(...) equals
+ * fa_bwd_ex(..., FA_DTYPE_F32, ...).
+ */
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, int o_dtype, const float* lse,
+                    const void* dO, float* dq, float* dk, float* dv, float* workspace, const int* seqlens_q,
+                    const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                    fa_stream_t stream);
 
 /*
  * Largest B*H*N that fa_bwd_noalloc accepts: 2^20 rows, i.e. 4 MiB of fp32

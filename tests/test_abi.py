@@ -116,6 +116,15 @@ def test_varlen_argument_errors(fa, call, args, expect):
     assert st == expect, fa.fa_status_string(st)
 
 
+@pytest.mark.parametrize("o_dtype,expect", [(2, 1), (-1, 1)])
+def test_output_dtype_errors(fa, o_dtype, expect):
+    st = fa.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, o_dtype, FAKE, 0, 0, 1, 1, 16, 16, 64, 0.125, 0, 0)
+    assert st == expect, fa.fa_status_string(st)
+    st = fa.fa_bwd_ex(FAKE, FAKE, FAKE, FAKE, o_dtype, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 1, 1, 16, 16, 64,
+                      0.125, 0, 0)
+    assert st == expect, fa.fa_status_string(st)
+
+
 def test_status_strings(fa):
     seen = set()
     for code in range(7):
