@@ -46,6 +46,7 @@ enum BwdSite : int {
   SITE_KV_EW_LD = 17,
   SITE_KV_EW_SDP = 18,
   SITE_KV_EW_ACC = 19,
+  SITE_KV_EW_DP = 20,
   SITE_Q_LOAD_Q = 21,
   SITE_Q_LOAD_KV = 22,
   SITE_Q_MMA_Q = 23,
@@ -54,6 +55,8 @@ enum BwdSite : int {
   SITE_Q_EW_SDP = 26,
   SITE_Q_EW_ACC = 27,
   SITE_Q_EW_XCH = 28,
+  SITE_Q_EW_DP = 29,
+  SITE_Q_MMA_P = 30,
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w, int site, int unit) {
@@ -150,8 +153,9 @@ struct KvLayout {
   static constexpr int QD_EMPTY = QD_FULL + kStages;
   static constexpr int LD_FULL = QD_EMPTY + kStages;
   static constexpr int LD_EMPTY = LD_FULL + kStages;
-  static constexpr int SDP_FULL = LD_EMPTY + kStages;
-  static constexpr int P_READY = SDP_FULL + 1;   // P^T stored (one arrive per elementwise warp)
+  static constexpr int S_FULL = LD_EMPTY + kStages;  // S^T computed
+  static constexpr int DP_FULL = S_FULL + 1;          // dP^T computed
+  static constexpr int P_READY = DP_FULL + 1;    // P^T stored (one arrive per elementwise warp)
   static constexpr int DS_READY = P_READY + 1;   // dS^T hi/lo stored
   static constexpr int ACC_FULL = DS_READY + 1;
   static constexpr int DRAIN = ACC_FULL + 1;
@@ -200,7 +204,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       mbar_init(bars + 8 * (L::LD_FULL + s), 1);    // the loader warp
       mbar_init(bars + 8 * (L::LD_EMPTY + s), 8);   // one per elementwise warp
     }
-    mbar_init(bars + 8 * L::SDP_FULL, 1);
+    mbar_init(bars + 8 * L::S_FULL, 1);
+    mbar_init(bars + 8 * L::DP_FULL, 1);
     mbar_init(bars + 8 * L::P_READY, 8);
     mbar_init(bars + 8 * L::DS_READY, 8);
     mbar_init(bars + 8 * L::ACC_FULL, 1);
@@ -245,7 +250,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const uint32_t ls = ldn % S;
         ok = warp_wait(BAR(L::LD_FULL + ls), (ldn / S) & 1, wc, SITE_KV_EW_LD, unit);
         if (!ok) break;
-        ok = warp_wait(BAR(L::SDP_FULL), sn & 1, wc, SITE_KV_EW_SDP, unit);
+        // P^T needs only S^T: dP^T may still be in the tensor pipe
+        const uint32_t sdp_parity = sn & 1;
+        ok = warp_wait(BAR(L::S_FULL), sdp_parity, wc, SITE_KV_EW_SDP, unit);
         if (!ok) break;
         ++sn;
         tc_fence_after();
@@ -310,7 +317,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           if (need_mask) pchunk(std::true_type{}, s1, 64 * w + 32, pk);
           else pchunk(std::false_type{}, s1, 64 * w + 32, pk);
           tmem_st16(tS + 16, pk);
-          tmem_ld32(tD, d0);  // dP arrives while P is being published
+          ok = warp_wait(BAR(L::DP_FULL), sdp_parity, wc, SITE_KV_EW_DP, unit);
+          if (!ok) {
+            tmem_st_wait();  // let the P stores land before leaving
+            break;
+          }
+          tc_fence_after();
+          tmem_ld32(tD, d0);  // dP^T arrives while P^T is being published
           tmem_ld32(tD + 32, d1);
           tmem_st_wait();
           tc_fence_before();
@@ -460,13 +473,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             umma_ss(tmem + L::kColS, sdesc_sw128(sbase + L::kKOff + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
                     id_s, ks > 0 ? 1u : 0u);
           }
+          umma_commit(BAR(L::S_FULL));
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
             umma_ss(tmem + L::kColDP, sdesc_sw128(sbase + L::kVOff + off, 16, 1024),
                     sdesc_sw128(da + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
           }
-          umma_commit(BAR(L::SDP_FULL));
+          umma_commit(BAR(L::DP_FULL));
           // dV += P^T dO and dK += dS^T Q: M = 128 keys, N = d, K = 128 queries.
           // P^T / dS^T of queries [64 w, 64 w + 64) sit in the first 32 columns of
           // the warpgroup's 64-column slice.  dV only needs P^T, published first.
@@ -566,8 +580,10 @@ struct QLayout {
   static constexpr int Q_EMPTY = 1;
   static constexpr int KV_FULL = 2;
   static constexpr int KV_EMPTY = KV_FULL + kStages;
-  static constexpr int SDP_FULL = KV_EMPTY + kStages;
-  static constexpr int DS_FULL = SDP_FULL + 1;
+  static constexpr int S_FULL = KV_EMPTY + kStages;  // S computed
+  static constexpr int DP_FULL = S_FULL + 1;          // dP computed
+  static constexpr int P_READY = DP_FULL + 1;         // P stored (one arrive per elementwise warp)
+  static constexpr int DS_FULL = P_READY + 1;
   static constexpr int ACC_FULL = DS_FULL + 1;
   static constexpr int XCH = ACC_FULL + 1;
   static constexpr int DRAIN = XCH + 1;
@@ -609,7 +625,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
       mbar_init(bars + 8 * (L::KV_FULL + s), 1);
       mbar_init(bars + 8 * (L::KV_EMPTY + s), 1);
     }
-    mbar_init(bars + 8 * L::SDP_FULL, 1);
+    mbar_init(bars + 8 * L::S_FULL, 1);
+    mbar_init(bars + 8 * L::DP_FULL, 1);
+    mbar_init(bars + 8 * L::P_READY, 8);
     mbar_init(bars + 8 * L::DS_FULL, 8);
     mbar_init(bars + 8 * L::ACC_FULL, 1);
     mbar_init(bars + 8 * L::XCH, 8);
@@ -679,7 +697,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const uint64_t dd2 = f2_pack(dd, dd);
       float dsum = 0.f;  // this warpgroup's share of delta_i
       for (int jt = 0; jt < nk; ++jt) {
-        ok = warp_wait(BAR(L::SDP_FULL), sn & 1, wc, SITE_Q_EW_SDP, unit);
+        // P needs only S: dP may still be in the tensor pipe
+        const uint32_t sdp_parity = sn & 1;
+        ok = warp_wait(BAR(L::S_FULL), sdp_parity, wc, SITE_Q_EW_SDP, unit);
         if (!ok) break;
         ++sn;
         tc_fence_after();
@@ -688,14 +708,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
         // number of eligible key columns of this tile for this row
         const bool need_mask = diag || tail;
         const int lim = need_mask ? ((CAUSAL ? min(row + hl.off + 1, hl.lk) : hl.lk) - jt * kTileRows) : kTileRows;
-        // MASKED: a tile crossing the causal boundary or holding the last
-        // valid key, where some key columns are not eligible
-        auto chunk = [&](auto masked, const uint32_t (&sr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&pk)[16],
-                         uint32_t (&hk)[16], uint32_t (&lk)[16]) {
-          uint64_t acc = f2_pack(0.f, 0.f);
+        // Phase 1: P for 32 key columns starting at col0, kept in sr as fp32
+        // bits and packed to bf16 in pk.  MASKED: a tile crossing the causal
+        // boundary or holding the last valid key, where some key columns are
+        // not eligible.
+        auto pchunk = [&](auto masked, uint32_t (&sr)[32], int col0, uint32_t (&pk)[16]) {
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            float p0, p1, ds0, ds1;
+            float p0, p1;
             f2_unpack(ffma2(f2_from(sr[c], sr[c + 1]), c2, nl2x2), p0, p1);
             p0 = ex2_approx(p0);
             p1 = ex2_approx(p1);
@@ -703,34 +723,59 @@ __global__ void __launch_bounds__(kQThreads, 1)
               if (col0 + c >= lim) p0 = 0.f;
               if (col0 + c + 1 >= lim) p1 = 0.f;
             }
-            const uint64_t ds01 = fmul2(f2_pack(p0, p1), fsub2(f2_from(dr[c], dr[c + 1]), dd2));
+            sr[c] = __float_as_uint(p0);
+            sr[c + 1] = __float_as_uint(p1);
+            pk[c / 2] = pack_bf16x2(p0, p1);
+          }
+        };
+        // Phase 2: dS = P o (dP - D), its row sum, and its hi + lo split
+        auto dchunk = [&](const uint32_t (&pr)[32], const uint32_t (&dr)[32], uint32_t (&hk)[16], uint32_t (&lk)[16]) {
+          uint64_t acc = f2_pack(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float ds0, ds1;
+            const uint64_t ds01 = fmul2(f2_from(pr[c], pr[c + 1]), fsub2(f2_from(dr[c], dr[c + 1]), dd2));
             acc = fadd2(acc, ds01);
             f2_unpack(ds01, ds0, ds1);
-            pk[c / 2] = pack_bf16x2(p0, p1);
             split_bf16x2(ds0, ds1, hk[c / 2], lk[c / 2]);
           }
           float a0, a1;
           f2_unpack(acc, a0, a1);
           dsum += a0 + a1;
         };
-        // Each store lands on columns this thread has already read.
+        // After use the warpgroup's slice holds P in S cols [64w, 64w+32),
+        // dS lo in S cols [64w+32, 64w+64) and dS hi in dP cols [64w, 64w+32);
+        // each store lands on columns this thread has already read.  P is
+        // published first so that B += P K queues behind dP in the tensor pipe.
         const uint32_t tS = tmem + lane_off + L::kColS + 64 * w;
         const uint32_t tD = tmem + lane_off + L::kColDP + 64 * w;
         {
           uint32_t s0[32], s1[32], d0[32], d1[32], pk[16], hk[16], lk[16];
           tmem_ld32(tS, s0);
           tmem_ld32(tS + 32, s1);
-          tmem_ld32(tD, d0);
-          tmem_ld32(tD + 32, d1);
           tmem_ld_wait();
-          if (need_mask) chunk(std::true_type{}, s0, d0, 64 * w, pk, hk, lk);
-          else chunk(std::false_type{}, s0, d0, 64 * w, pk, hk, lk);
+          if (need_mask) pchunk(std::true_type{}, s0, 64 * w, pk);
+          else pchunk(std::false_type{}, s0, 64 * w, pk);
           tmem_st16(tS, pk);
+          if (need_mask) pchunk(std::true_type{}, s1, 64 * w + 32, pk);
+          else pchunk(std::false_type{}, s1, 64 * w + 32, pk);
+          tmem_st16(tS + 16, pk);
+          ok = warp_wait(BAR(L::DP_FULL), sdp_parity, wc, SITE_Q_EW_DP, unit);
+          if (!ok) {
+            tmem_st_wait();  // let the P stores land before leaving
+            break;
+          }
+          tc_fence_after();
+          tmem_ld32(tD, d0);  // dP arrives while P is being published
+          tmem_ld32(tD + 32, d1);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive_warp(BAR(L::P_READY));
+          tmem_ld_wait();
+          dchunk(s0, d0, hk, lk);
           tmem_st16(tD, hk);
           tmem_st16(tS + 32, lk);
-          if (need_mask) chunk(std::true_type{}, s1, d1, 64 * w + 32, pk, hk, lk);
-          else chunk(std::false_type{}, s1, d1, 64 * w + 32, pk, hk, lk);
-          tmem_st16(tS + 16, pk);
+          dchunk(s1, d1, hk, lk);
           tmem_st16(tD + 16, hk);
           tmem_st16(tS + 48, lk);
         }
@@ -853,13 +898,24 @@ __global__ void __launch_bounds__(kQThreads, 1)
             umma_ss(tmem + L::kColS, sdesc_sw128(sbase + L::kQOff + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
                     id_s, ks > 0 ? 1u : 0u);
           }
+          umma_commit(BAR(L::S_FULL));
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
             umma_ss(tmem + L::kColDP, sdesc_sw128(sbase + L::kDoOff + off, 16, 1024),
                     sdesc_sw128(va + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
           }
-          umma_commit(BAR(L::SDP_FULL));
+          umma_commit(BAR(L::DP_FULL));
+          // B += P K as soon as P is stored, for the delta correction
+          ok = wait_bounded(BAR(L::P_READY), dn & 1, wc, SITE_Q_MMA_P, unit);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
+            umma_ts(tmem + L::kColB, tmem + L::kColS + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
+                    id_acc, (jt > 0 || ks > 0) ? 1u : 0u);
+          }
           ok = wait_bounded(BAR(L::DS_FULL), dn & 1, wc, SITE_Q_MMA_DS, unit);
           if (!ok) break;
           ++dn;
@@ -876,12 +932,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
             const uint32_t acol = 32 + 64 * (ks >> 2) + 8 * (ks & 3);
             umma_ts(tmem + L::kColDQ, tmem + L::kColS + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
                     id_acc, 1u);
-          }
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {  // B += P K, for the delta correction
-            const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColB, tmem + L::kColS + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
-                    id_acc, (jt > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit(BAR(L::KV_EMPTY + s));
           ++kvpos;
