@@ -299,11 +299,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           }
         };
         // Column slice of this warpgroup: S^T [64w, 64w+64), dP^T likewise.
-        // After use the slice holds P^T in S cols [64w, 64w+32), dS^T lo in
-        // S cols [64w+32, 64w+64) and dS^T hi in dP cols [64w, 64w+32); every
-        // store lands on columns this thread has already read.  P^T is
-        // published first so the MMA thread can run dV += P^T dO while dS^T is
-        // still being computed.
+        // After use the slice holds P^T in S cols [64w, 64w+32) and dS^T hi
+        // and lo in dP cols [64w, 64w+32) and [64w+32, 64w+64); every store
+        // lands on columns this thread has already read.  P^T is published
+        // first so the MMA thread can run dV += P^T dO, and then S^T of the
+        // next query tile, while dS^T is still being computed.
         const uint32_t tS = tmem + lane_off + L::kColS + 64 * w;
         const uint32_t tD = tmem + lane_off + L::kColDP + 64 * w;
         {
@@ -331,10 +331,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           tmem_ld_wait();
           dchunk(s0, d0, 64 * w, hk, lk);
           tmem_st16(tD, hk);
-          tmem_st16(tS + 32, lk);
+          tmem_st16(tD + 32, lk);
           dchunk(s1, d1, 64 * w + 32, hk, lk);
           tmem_st16(tD + 16, hk);
-          tmem_st16(tS + 48, lk);
+          tmem_st16(tD + 48, lk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -459,14 +459,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         ok = wait_bounded(BAR(L::KV_FULL), kvn & 1, wc, SITE_KV_MMA_KV, unit);
         if (!ok) break;
         ++kvn;
-        for (int i = i0; i < i1; ++i) {
-          const uint32_t s = qdpos % S;
-          ok = wait_bounded(BAR(L::QD_FULL + s), (qdpos / S) & 1, wc, SITE_KV_MMA_QD, unit);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t qa = sbase + L::kQdOff + s * 2 * L::kTileBytes;
-          const uint32_t da = qa + L::kTileBytes;
-          // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = 128 queries, K = d
+        // S^T = K Q^T and dP^T = V dO^T of one query tile: M = 128 keys,
+        // N = 128 queries, K = d
+        auto issue_s = [&](uint32_t qa) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -474,6 +469,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::S_FULL));
+        };
+        auto issue_dp = [&](uint32_t da) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -481,9 +478,25 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     sdesc_sw128(da + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::DP_FULL));
-          // dV += P^T dO and dK += dS^T Q: M = 128 keys, N = d, K = 128 queries.
-          // P^T / dS^T of queries [64 w, 64 w + 64) sit in the first 32 columns of
-          // the warpgroup's 64-column slice.  dV only needs P^T, published first.
+        };
+        auto stage_addr = [&](uint32_t pos) { return sbase + L::kQdOff + (pos % S) * 2 * L::kTileBytes; };
+        ok = wait_bounded(BAR(L::QD_FULL + qdpos % S), (qdpos / S) & 1, wc, SITE_KV_MMA_QD, unit);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(stage_addr(qdpos));
+        issue_dp(stage_addr(qdpos) + L::kTileBytes);
+        // Per query tile i: dV += P^T dO once P^T is stored; then S^T of tile
+        // i+1, which overwrites P^T(i) only after dV(i) has read it (the
+        // tensor pipe runs in issue order), so the elementwise warps find
+        // S^T(i+1) ready when they finish tile i; then dK += dS^T Q (hi and
+        // lo, both in the dP^T columns); then dP^T of tile i+1, behind dK(i).
+        // M = 128 keys, N = d, K = 128 queries; the warpgroup w's P^T sits in
+        // S columns [64 w, 64 w + 32), its dS^T hi and lo in dP columns
+        // [64 w, 64 w + 32) and [64 w + 32, 64 w + 64).
+        for (int i = i0; i < i1; ++i) {
+          const uint32_t s = qdpos % S;
+          const uint32_t qa = stage_addr(qdpos);
+          const uint32_t da = qa + L::kTileBytes;
           ok = wait_bounded(BAR(L::P_READY), pn & 1, wc, SITE_KV_MMA_PDS, unit);
           if (!ok) break;
           tc_fence_after();
@@ -493,6 +506,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
             umma_ts(tmem + L::kColDV, tmem + L::kColS + acol, sdesc_sw128(da + ks * 2048, kTileRows * 128, 1024),
                     id_acc, (!first || ks > 0) ? 1u : 0u);
+          }
+          const bool more = i + 1 < i1;
+          if (more) {
+            ok = wait_bounded(BAR(L::QD_FULL + (qdpos + 1) % S), ((qdpos + 1) / S) & 1, wc, SITE_KV_MMA_QD, unit);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(stage_addr(qdpos + 1));
           }
           ok = wait_bounded(BAR(L::DS_READY), pn & 1, wc, SITE_KV_MMA_PDS, unit);
           if (!ok) break;
@@ -507,11 +527,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {  // dS^T lo part
             const uint32_t acol = 32 + 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDK, tmem + L::kColS + acol, sdesc_sw128(qa + ks * 2048, kTileRows * 128, 1024),
+            umma_ts(tmem + L::kColDK, tmem + L::kColDP + acol, sdesc_sw128(qa + ks * 2048, kTileRows * 128, 1024),
                     id_acc, 1u);
           }
           umma_commit(BAR(L::QD_EMPTY + s));
           ++qdpos;
+          if (more) issue_dp(stage_addr(qdpos) + L::kTileBytes);
         }
         if (!ok) break;
         umma_commit(BAR(L::ACC_FULL));
@@ -590,8 +611,8 @@ struct QLayout {
   static constexpr int kNumBars = DRAIN + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
-  // S [0,128): after use P (bf16) in each warpgroup's first 32 columns and
-  // dS lo in its last 32; dP [128,256): dS hi in each warpgroup's first 32;
+  // S [0,128): after use P (bf16) in each warpgroup's first 32 columns;
+  // dP [128,256): dS hi in each warpgroup's first 32 and dS lo in its last 32;
   // dQ accumulator [256, 256+d); B = sum_j P_ij k_j accumulator [256+d, 256+2d).
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColB = 256 + D;
 };
@@ -743,10 +764,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
           f2_unpack(acc, a0, a1);
           dsum += a0 + a1;
         };
-        // After use the warpgroup's slice holds P in S cols [64w, 64w+32),
-        // dS lo in S cols [64w+32, 64w+64) and dS hi in dP cols [64w, 64w+32);
-        // each store lands on columns this thread has already read.  P is
-        // published first so that B += P K queues behind dP in the tensor pipe.
+        // After use the warpgroup's slice holds P in S cols [64w, 64w+32) and
+        // dS hi and lo in dP cols [64w, 64w+32) and [64w+32, 64w+64); each
+        // store lands on columns this thread has already read.  P is published
+        // first so that B += P K, and then S of the next key tile, queue
+        // behind dP in the tensor pipe.
         const uint32_t tS = tmem + lane_off + L::kColS + 64 * w;
         const uint32_t tD = tmem + lane_off + L::kColDP + 64 * w;
         {
@@ -774,10 +796,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
           tmem_ld_wait();
           dchunk(s0, d0, hk, lk);
           tmem_st16(tD, hk);
-          tmem_st16(tS + 32, lk);
+          tmem_st16(tD + 32, lk);
           dchunk(s1, d1, hk, lk);
           tmem_st16(tD + 16, hk);
-          tmem_st16(tS + 48, lk);
+          tmem_st16(tD + 48, lk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -884,14 +906,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
         ok = wait_bounded(BAR(L::Q_FULL), qn & 1, wc, SITE_Q_MMA_Q, unit);
         if (!ok) break;
         ++qn;
-        for (int jt = 0; jt < nk; ++jt) {
-          const uint32_t s = kvpos % S;
-          ok = wait_bounded(BAR(L::KV_FULL + s), (kvpos / S) & 1, wc, SITE_Q_MMA_KV, unit);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t ka = sbase + L::kKvOff + s * 2 * L::kTileBytes;
-          const uint32_t va = ka + L::kTileBytes;
-          // S = Q K^T and dP = dO V^T: M = 128 queries, N = 128 keys, K = d
+        // S = Q K^T and dP = dO V^T of one key tile: M = 128 queries,
+        // N = 128 keys, K = d
+        auto issue_s = [&](uint32_t ka) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -899,6 +916,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
                     id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::S_FULL));
+        };
+        auto issue_dp = [&](uint32_t va) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -906,21 +925,43 @@ __global__ void __launch_bounds__(kQThreads, 1)
                     sdesc_sw128(va + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::DP_FULL));
-          // B += P K as soon as P is stored, for the delta correction
+        };
+        auto kv_addr = [&](uint32_t pos) { return sbase + L::kKvOff + (pos % S) * 2 * L::kTileBytes; };
+        ok = wait_bounded(BAR(L::KV_FULL + kvpos % S), (kvpos / S) & 1, wc, SITE_Q_MMA_KV, unit);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(kv_addr(kvpos));
+        issue_dp(kv_addr(kvpos) + L::kTileBytes);
+        // Per key tile jt: B += P K once P is stored; then S of tile jt+1,
+        // which overwrites P(jt) only after B(jt) has read it (the tensor
+        // pipe runs in issue order); then dQ += dS K (hi and lo, both in the
+        // dP columns); then dP of tile jt+1, behind dQ(jt).  M = 128 queries,
+        // N = d, K = 128 keys, K tile MN-major; the warpgroup w's P sits in S
+        // columns [64 w, 64 w + 32), its dS hi and lo in dP columns
+        // [64 w, 64 w + 32) and [64 w + 32, 64 w + 64).
+        for (int jt = 0; jt < nk; ++jt) {
+          const uint32_t s = kvpos % S;
+          const uint32_t ka = kv_addr(kvpos);
           ok = wait_bounded(BAR(L::P_READY), dn & 1, wc, SITE_Q_MMA_P, unit);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
+          for (int ks = 0; ks < 8; ++ks) {  // B += P K, for the delta correction
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
             umma_ts(tmem + L::kColB, tmem + L::kColS + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
                     id_acc, (jt > 0 || ks > 0) ? 1u : 0u);
+          }
+          const bool more = jt + 1 < nk;
+          if (more) {
+            ok = wait_bounded(BAR(L::KV_FULL + (kvpos + 1) % S), ((kvpos + 1) / S) & 1, wc, SITE_Q_MMA_KV, unit);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(kv_addr(kvpos + 1));
           }
           ok = wait_bounded(BAR(L::DS_FULL), dn & 1, wc, SITE_Q_MMA_DS, unit);
           if (!ok) break;
           ++dn;
           tc_fence_after();
-          // dQ += dS K: M = 128 queries, N = d, K = 128 keys; K tile MN-major
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
@@ -930,11 +971,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {  // dS lo part
             const uint32_t acol = 32 + 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDQ, tmem + L::kColS + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
+            umma_ts(tmem + L::kColDQ, tmem + L::kColDP + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
                     id_acc, 1u);
           }
           umma_commit(BAR(L::KV_EMPTY + s));
           ++kvpos;
+          if (more) issue_dp(kv_addr(kvpos) + L::kTileBytes);
         }
         if (!ok) break;
         umma_commit(BAR(L::ACC_FULL));
