@@ -168,12 +168,13 @@ struct KvLayout {
 
 // 12 warps: two elementwise warpgroups, then TMA (warp 8), MMA (warp 9), the
 // LSE/D loader (warp 10) and an idle warp completing the third warpgroup.
-// Launched at 168 registers a thread; the elementwise warpgroups take 192 and
-// the third keeps 120 (2*128*192 + 128*120 = 384*168).
+// Launched at 168 registers a thread; the elementwise warpgroups take 184 and
+// the third keeps 136 (2*128*184 + 128*136 = 384*168), enough for the MMA
+// thread to hold its descriptors without spilling.
 constexpr int kKvThreads = 384;
 constexpr int kKvLaunchRegs = 168;
-constexpr int kKvEwRegs = 192;
-constexpr int kKvOtherRegs = 120;
+constexpr int kKvEwRegs = 184;
+constexpr int kKvOtherRegs = 136;
 static_assert(2 * 128 * kKvEwRegs + 128 * kKvOtherRegs <= kKvThreads * kKvLaunchRegs,
               "register split exceeds the launch allocation");
 
