@@ -182,6 +182,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, status, limit_ns};
   const int nq = geom.nq;
+  // bf16 output is served by the general (VARLEN) instantiation only, so the
+  // square fp32 kernel carries no output-type branch
+  const bool obf16 = VARLEN && o_bf16;
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
 
   if (warp < 8) {
@@ -208,9 +211,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (row < nq) {
           // D fp32 or D bf16 zeros: 4 D or 2 D bytes, in 16-byte stores
           uint4* orow = reinterpret_cast<uint4*>(static_cast<uint8_t*>(o) +
-                                                 (static_cast<size_t>(head) * nq + row) * D * (o_bf16 ? 2 : 4));
+                                                 (static_cast<size_t>(head) * nq + row) * D * (obf16 ? 2 : 4));
 #pragma unroll 1
-          for (int c = 0; c < (o_bf16 ? D / 8 : D / 4); ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
+          for (int c = 0; c < (obf16 ? D / 8 : D / 4); ++c) orow[c] = make_uint4(0u, 0u, 0u, 0u);
           lse[static_cast<size_t>(head) * nq + row] = -CUDART_INF_F;
         }
         continue;
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        if (valid && o_bf16) {
+        if (valid && obf16) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint4 h;
@@ -534,7 +537,7 @@ cudaError_t launch_fwd_v(const FwdArgs& a, cudaStream_t stream) {
 
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
-  const bool square = !a.geom.seqlens_q && !a.geom.seqlens_k && a.geom.nq == a.geom.nk;
+  const bool square = !a.geom.seqlens_q && !a.geom.seqlens_k && a.geom.nq == a.geom.nk && !a.o_bf16;
   return square ? launch_fwd_v<D, CAUSAL, false>(a, stream) : launch_fwd_v<D, CAUSAL, true>(a, stream);
 }
 
