@@ -318,17 +318,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           if (need_mask) pchunk(std::true_type{}, s1, 64 * w + 32, pk);
           else pchunk(std::false_type{}, s1, 64 * w + 32, pk);
           tmem_st16(tS + 16, pk);
-          ok = warp_wait(BAR(L::DP_FULL), sdp_parity, wc, SITE_KV_EW_DP, unit);
-          if (!ok) {
-            tmem_st_wait();  // let the P stores land before leaving
-            break;
-          }
-          tc_fence_after();
-          tmem_ld32(tD, d0);  // dP^T arrives while P^T is being published
-          tmem_ld32(tD + 32, d1);
+          // publish P before taking dP, so that the GEMM reading P (and the
+          // next tile's S behind it) queue up while dP is still running
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive_warp(BAR(L::P_READY));
+          ok = warp_wait(BAR(L::DP_FULL), sdp_parity, wc, SITE_KV_EW_DP, unit);
+          if (!ok) break;
+          tc_fence_after();
+          tmem_ld32(tD, d0);
+          tmem_ld32(tD + 32, d1);
           tmem_ld_wait();
           dchunk(s0, d0, 64 * w, hk, lk);
           tmem_st16(tD, hk);
@@ -783,17 +782,16 @@ __global__ void __launch_bounds__(kQThreads, 1)
           if (need_mask) pchunk(std::true_type{}, s1, 64 * w + 32, pk);
           else pchunk(std::false_type{}, s1, 64 * w + 32, pk);
           tmem_st16(tS + 16, pk);
-          ok = warp_wait(BAR(L::DP_FULL), sdp_parity, wc, SITE_Q_EW_DP, unit);
-          if (!ok) {
-            tmem_st_wait();  // let the P stores land before leaving
-            break;
-          }
-          tc_fence_after();
-          tmem_ld32(tD, d0);  // dP arrives while P is being published
-          tmem_ld32(tD + 32, d1);
+          // publish P before taking dP, so that the GEMM reading P (and the
+          // next tile's S behind it) queue up while dP is still running
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive_warp(BAR(L::P_READY));
+          ok = warp_wait(BAR(L::DP_FULL), sdp_parity, wc, SITE_Q_EW_DP, unit);
+          if (!ok) break;
+          tc_fence_after();
+          tmem_ld32(tD, d0);
+          tmem_ld32(tD + 32, d1);
           tmem_ld_wait();
           dchunk(s0, d0, hk, lk);
           tmem_st16(tD, hk);
