@@ -2,7 +2,7 @@
 """Attention TFLOP/s on GB300: forward + backward of exact tiled attention.
 
 One step is one pass of the whole path over one batch: fa_fwd (O, LSE) then
-the three kernels of fa_bwd (D preprocess, dQ, dK/dV), each through its own
+the two kernels of fa_bwd (dQ with the row term D, then dK/dV), each through its own
 C call so that each kernel is timed with CUDA events on the stream.  Counted FLOPs: 4*B*H*N^2*d for the
 forward, halved when causal, and 2.5x that for the backward.  Default
 workload: B=4, H=16, N=8192, d=128, causal, bf16 inputs ~ N(0,1).
@@ -71,7 +71,6 @@ def load_peaks():
 
 KERNEL_SOURCES = {
     "fwd_kernel": ["fwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
-    "preprocess_kernel": ["bwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
     "dq_kernel": ["bwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
     "dkdv_kernel": ["bwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
     "decode_kernel": ["decode.cu", "geom.cuh", "ptx.cuh", "internal.h"],
@@ -258,10 +257,10 @@ def run_ours(args):
         dq, dk, dv = (torch.empty((B, H, N, d), dtype=torch.float32, device=device) for _ in range(3))
         ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N) // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
-    launches_per_step = 1 + (3 if do_bwd else 0)
+    launches_per_step = 1 + (2 if do_bwd else 0)
 
     ev = []
-    nev = 5 if do_bwd else 2
+    nev = 4 if do_bwd else 2
 
     def step(record):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(nev)] if record else None
@@ -272,7 +271,7 @@ def run_ours(args):
             e[1].record(stream)
         if do_bwd:
             # fa_bwd's three kernels, one C call each so each can be timed
-            for stage in range(3):
+            for stage in range(2):
                 fa.backward_stage(stage, q, k, v, o, lse, dout, dq, dk, dv, ws, causal=w.causal, scale=w.scale)
                 if record:
                     e[2 + stage].record(stream)
@@ -356,15 +355,12 @@ def run_ours(args):
     bwd_tflops = w.bwd_flops() / (bwd_ms * 1e-3) / 1e12 if do_bwd else None
     # Algorithmic work per launch of each kernel (one launch covers the whole
     # batch): forward 2 GEMMs (S, PV); dQ 3 (S, dP, dQ); dK/dV 4 (S, dP, dV,
-    # dK), each 2*N^2*d per head, halved under the causal mask; the
-    # preprocess moves dO (bf16) and O (fp32) in and D (fp32) out.
+    # dK), each 2*N^2*d per head, halved under the causal mask.
     gemm = w.fwd_flops() / 2
-    rows = w.B * w.H * w.N
     kernels = [("fwd_kernel", fwd_ms, "tensor", 2 * gemm)]
     if do_bwd:
-        kernels += [("preprocess_kernel", kern_ms[1], "hbm", rows * (w.d * 6 + 4)),
-                    ("dq_kernel", kern_ms[2], "tensor", 3 * gemm),
-                    ("dkdv_kernel", kern_ms[3], "tensor", 4 * gemm)]
+        kernels += [("dq_kernel", kern_ms[1], "tensor", 3 * gemm),
+                    ("dkdv_kernel", kern_ms[2], "tensor", 4 * gemm)]
     name, ms, bound, work = max(kernels, key=lambda t: t[1])
     if bound == "tensor":
         achieved, peak, unit = work / (ms * 1e-3) / 1e12, sustained, "TFLOP/s"

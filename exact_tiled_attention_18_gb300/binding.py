@@ -139,7 +139,7 @@ def fa_bwd_varlen(q: int, k: int, v: int, o: int, lse: int, do: int, dq: int, dk
 
 def fa_bwd_stage(stage: int, q: int, k: int, v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int,
                  workspace: int, B: int, H: int, N: int, d: int, scale: float, causal: int, stream: int) -> int:
-    """Raw C call of one backward stage (0 preprocess, 1 dQ, 2 dK/dV)."""
+    """Raw C call of one backward stage (0 dQ and the row term, 1 dK/dV)."""
     return lib().fa_bwd_stage(stage, q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, N, d, scale, causal, stream)
 
 

@@ -212,7 +212,6 @@ fa_status bwd_prepare(fa::BwdArgs& a, const void* q, const void* k, const void* 
   a.sched_q = make_sched(heads, Nq, d, causal, di.sms, 0, fa::kTileRows, 1, Nk);
   a.grid_kv = a.sched_kv.grid;
   a.grid_q = a.sched_q.grid;
-  a.grid_pre = 2 * di.sms;
   a.status = di.status;
   a.wait_limit_ns = wait_limit_ns();
   return FA_OK;
@@ -388,7 +387,7 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const floa
       if (cudaGetSymbolAddress(&p, g_fa_noalloc_delta) != cudaSuccess || !p) return FA_ERR_LAUNCH;
       g_noalloc_ptr[dev] = static_cast<float*>(p);
     }
-    a.delta = g_noalloc_ptr[dev];  // every row is written by the preprocess kernel before it is read
+    a.delta = g_noalloc_ptr[dev];  // every row is written by the dQ kernel before dK/dV reads it
   }
   return fa::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
@@ -396,7 +395,7 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const floa
 fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const float* o, const float* lse,
                        const void* dO, float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d,
                        float scale, int causal, fa_stream_t stream) {
-  if (stage < 0 || stage > 2 || !workspace) return FA_ERR_INVALID_ARG;
+  if (stage < 0 || stage > 1 || !workspace) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a;
   fa_status st =
       bwd_prepare(a, q, k, v, o, FA_DTYPE_F32, lse, dO, dq, dk, dv, workspace, nullptr, nullptr, B, H, N, N, d, scale,

@@ -9,18 +9,18 @@
 //   dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
 // (D_i = sum_j P_ij dP_ij equals rowsum(dO o O) because O = P V.)
 //
-// Three kernels, in stream order:
-//   preprocess  D' = rowsum(dO o O)                        (HBM bound)
+// Two kernels, in stream order:
+//   dq          one CTA per 128-query tile, sweeping its key tiles:
+//               S = Q K^T, dP = dO V^T, dS (hi + lo) in TMEM, dQ += dS K;
+//               a loader warp forms D' = rowsum(dO o O) one unit ahead, and
+//               the kernel corrects D' to the exact row term (see the
+//               kernel), so it runs before dkdv.
 //   dkdv        one CTA per 128-key tile, sweeping the query tiles that
 //               see it: S^T = K Q^T and dP^T = V dO^T on tcgen05 into TMEM,
 //               P^T and dS^T computed by two warpgroups (thread = key row)
 //               and written back to TMEM as bf16 (dS^T as a hi + lo pair),
 //               then dV += P^T dO and dK += (dS^T hi + dS^T lo) Q with the A
 //               operand read from TMEM.
-//   dq          one CTA per 128-query tile, sweeping its key tiles:
-//               S = Q K^T, dP = dO V^T, dS (hi + lo) in TMEM, dQ += dS K;
-//               it also corrects D' to the exact row term (see the kernel)
-//               and so runs before dkdv.
 // Every pipeline wait is bounded, as in the forward kernel.
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -57,6 +57,8 @@ enum BwdSite : int {
   SITE_Q_EW_XCH = 28,
   SITE_Q_EW_DP = 29,
   SITE_Q_MMA_P = 30,
+  SITE_Q_EW_DD = 31,
+  SITE_Q_DD_EMPTY = 32,
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w, int site, int unit) {
@@ -90,50 +92,6 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, u
 
 __device__ __forceinline__ uint64_t f2_from(uint32_t a, uint32_t b) {
   return f2_pack(__uint_as_float(a), __uint_as_float(b));
-}
-
-// ------------------------------------------------------------------ preprocess
-// D_i = sum_c dO_ic O_ic.  d/8 threads per row, 8 elements per thread; the
-// loop bound is uniform across a warp so every lane reaches the shuffles.
-// O is fp32, or bf16 when OBF16.
-template <int D, bool OBF16>
-__global__ void __launch_bounds__(256) preprocess_kernel(const void* __restrict__ o_,
-                                                         const uint16_t* __restrict__ dout,
-                                                         float* __restrict__ delta, const int rows) {
-  constexpr int G = D / 8;            // threads per row
-  constexpr int kRowsPerWarp = 32 / G;
-  const int sub = threadIdx.x % G;
-  const int gi = (threadIdx.x & 31) / G;
-  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nwarps = (gridDim.x * blockDim.x) >> 5;
-  for (int base = warp_global * kRowsPerWarp; base < rows; base += nwarps * kRowsPerWarp) {
-    const int row = base + gi;
-    float acc = 0.f;
-    if (row < rows) {
-      const uint4 h = __ldg(reinterpret_cast<const uint4*>(dout + static_cast<size_t>(row) * D) + sub);
-      float4 a, b;
-      if constexpr (OBF16) {
-        const uint4 oh =
-            __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o_) + static_cast<size_t>(row) * D) + sub);
-        a = make_float4(bf16_bits_to_float(oh.x & 0xFFFFu), bf16_bits_to_float(oh.x >> 16),
-                        bf16_bits_to_float(oh.y & 0xFFFFu), bf16_bits_to_float(oh.y >> 16));
-        b = make_float4(bf16_bits_to_float(oh.z & 0xFFFFu), bf16_bits_to_float(oh.z >> 16),
-                        bf16_bits_to_float(oh.w & 0xFFFFu), bf16_bits_to_float(oh.w >> 16));
-      } else {
-        const float4* op =
-            reinterpret_cast<const float4*>(static_cast<const float*>(o_) + static_cast<size_t>(row) * D) + 2 * sub;
-        a = __ldg(op);
-        b = __ldg(op + 1);
-      }
-      acc = a.x * bf16_bits_to_float(h.x & 0xFFFFu) + a.y * bf16_bits_to_float(h.x >> 16) +
-            a.z * bf16_bits_to_float(h.y & 0xFFFFu) + a.w * bf16_bits_to_float(h.y >> 16) +
-            b.x * bf16_bits_to_float(h.z & 0xFFFFu) + b.y * bf16_bits_to_float(h.z >> 16) +
-            b.z * bf16_bits_to_float(h.w & 0xFFFFu) + b.w * bf16_bits_to_float(h.w >> 16);
-    }
-#pragma unroll
-    for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (sub == 0 && row < rows) delta[row] = acc;
-  }
 }
 
 // ------------------------------------------------------------------ dK / dV
@@ -596,7 +554,8 @@ struct QLayout {
   static constexpr int kDoOff = kTileBytes;
   static constexpr int kKvOff = 2 * kTileBytes;  // stage s: K at +0, V at +kTileBytes
   static constexpr int kXchOff = kKvOff + kStages * 2 * kTileBytes;  // [2 units][2 warpgroups][128] fp32
-  static constexpr int kBarOff = kXchOff + 2 * 2 * 128 * 4;
+  static constexpr int kDdOff = kXchOff + 2 * 2 * 128 * 4;            // [2 units][128] fp32 row terms D'
+  static constexpr int kBarOff = kDdOff + 2 * 128 * 4;
   static constexpr int Q_FULL = 0;
   static constexpr int Q_EMPTY = 1;
   static constexpr int KV_FULL = 2;
@@ -607,7 +566,9 @@ struct QLayout {
   static constexpr int DS_FULL = P_READY + 1;
   static constexpr int ACC_FULL = DS_FULL + 1;
   static constexpr int XCH = ACC_FULL + 1;
-  static constexpr int DRAIN = XCH + 1;
+  static constexpr int DD_FULL = XCH + 1;       // 2 slots: D' of a unit written (two loader warps)
+  static constexpr int DD_EMPTY = DD_FULL + 2;  // 2 slots: D' read (one arrive per elementwise warp)
+  static constexpr int DRAIN = DD_EMPTY + 2;
   static constexpr int kNumBars = DRAIN + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
@@ -617,15 +578,17 @@ struct QLayout {
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColB = 256 + D;
 };
 
-// 12 warps: two elementwise warpgroups, TMA (warp 8), MMA (warp 9) and two idle
-// warps completing the third warpgroup; same register split as dK/dV.
+// 12 warps: two elementwise warpgroups, TMA (warp 8), MMA (warp 9) and the two
+// row-term loaders (warps 10, 11) completing the third warpgroup; same
+// register split as dK/dV.
 constexpr int kQThreads = 384;
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kQThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              const float* __restrict__ lse, float* __restrict__ delta, float* __restrict__ dq, const SeqGeom geom,
+              const float* __restrict__ lse, const void* __restrict__ o, const uint16_t* __restrict__ dout,
+              const int o_bf16, float* __restrict__ delta, float* __restrict__ dq, const SeqGeom geom,
               const float scale, const float scale_log2, const SchedParams sp, int* status,
               const unsigned long long limit_ns) {
   using L = QLayout<D>;
@@ -652,6 +615,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
     mbar_init(bars + 8 * L::DS_FULL, 8);
     mbar_init(bars + 8 * L::ACC_FULL, 1);
     mbar_init(bars + 8 * L::XCH, 8);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bars + 8 * (L::DD_FULL + s), 2);  // the two loader warps
+      mbar_init(bars + 8 * (L::DD_EMPTY + s), 8);
+    }
     mbar_init(bars + 8 * L::DRAIN, 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -676,17 +643,19 @@ __global__ void __launch_bounds__(kQThreads, 1)
   if (warp < 8) {
     // ------------------------------------------------- dS (thread = query row)
     regs_increase<kKvEwRegs>();
-    // The row term comes in as D'_i = rowsum(dO o O) with O from the forward
-    // pass, whose P was rounded to bf16 for the PV product.  The kernel sees
-    // every key of its rows, so it also sums delta_i = sum_j dS'_ij =
-    // sum_j P_ij dP_ij - D'_i in fp32, corrects its own product with
+    // The row term comes in as D'_i = rowsum(dO o O) (computed by the loader
+    // warp one unit ahead) with O from the forward pass, whose P was rounded
+    // to bf16 for the PV product.  The kernel sees every key of its rows, so
+    // it also sums delta_i = sum_j dS'_ij = sum_j P_ij dP_ij - D'_i in fp32,
+    // corrects its own product with
     // dQ = scale (sum_j dS'_ij k_j - delta_i sum_j P_ij k_j), and stores the
     // corrected D_i = D'_i + delta_i for the dK/dV kernel.
     const int w = warp >> 2;  // key columns [64 w, 64 w + 64)
     const int r = ((warp & 3) << 5) + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
     float* xch = reinterpret_cast<float*>(smem + L::kXchOff);
-    uint32_t sn = 0, an = 0;
+    const float* dd_s = reinterpret_cast<const float*>(smem + L::kDdOff);
+    uint32_t sn = 0, an = 0, ddn = 0;
     SchedIter it = sched_begin(sp);
     int head, i;
     bool ok = true;
@@ -711,7 +680,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const float lv = row < hl.lq ? lse[ridx] : -CUDART_INF_F;
       const bool has = lv > -CUDART_INF_F;  // a valid row with at least one key
       const float l2 = has ? lv * kLog2e : CUDART_INF_F;
-      const float dd = has ? delta[ridx] : 0.f;
+      ok = warp_wait(BAR(L::DD_FULL + (ddn & 1)), (ddn >> 1) & 1, wc, SITE_Q_EW_DD, unit);
+      if (!ok) break;
+      const float dd = has ? dd_s[(ddn & 1) * 128 + r] : 0.f;
+      mbar_arrive_warp(BAR(L::DD_EMPTY + (ddn & 1)));
+      ++ddn;
       const float nl2 = -l2;
       const uint64_t c2 = f2_pack(scale_log2, scale_log2);
       const uint64_t nl2x2 = f2_pack(nl2, nl2);
@@ -889,6 +862,88 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
       }
     }
+  } else if (warp >= 10) {
+    // ---------------------------- row term D'_i = sum_c dO_ic O_ic, one unit ahead
+    // Warps 10 and 11 take 64 rows each, 16 rows per step with all their
+    // loads in flight (O streams from HBM); within a row, lane l takes
+    // columns [CW l, CW l + CW) of O (fp32 or bf16) and dO, then a warp sum.
+    constexpr int CW = D / 32;
+    constexpr int kRowsPerStep = 16;
+    float* dds = reinterpret_cast<float*>(smem + L::kDdOff);
+    const int lw = warp - 10;
+    uint32_t ddn = 0;
+    SchedIter it = sched_begin(sp);
+    int head, i;
+    bool ok = true;
+    while (ok && sched_next(it, sp, blockIdx.x, head, i)) {
+      const HeadLen hl = head_len(geom, head);
+      if (query_tile_keys(hl, i, CAUSAL) == 0) continue;  // the elementwise warps skip it too
+      const int unit = head * sp.units_per_head + i;
+      ok = warp_wait(BAR(L::DD_EMPTY + (ddn & 1)), ((ddn >> 1) & 1) ^ 1, wc, SITE_Q_DD_EMPTY, unit);
+      if (!ok) break;
+      float* slot = dds + (ddn & 1) * 128;
+#pragma unroll 1
+      for (int r0 = 64 * lw; r0 < 64 * lw + 64; r0 += kRowsPerStep) {
+        float ov[kRowsPerStep][CW];
+        uint32_t dh[kRowsPerStep][CW / 2];
+#pragma unroll
+        for (int u = 0; u < kRowsPerStep; ++u) {
+          const int row = i * kTileRows + r0 + u;
+          const bool in = row < hl.lq;
+          const size_t base = (static_cast<size_t>(head) * geom.nq + (in ? row : 0)) * D + CW * lane;
+          if (o_bf16) {
+            const uint16_t* op = static_cast<const uint16_t*>(o) + base;
+            if constexpr (CW == 4) {
+              const uint2 h = in ? __ldg(reinterpret_cast<const uint2*>(op)) : make_uint2(0u, 0u);
+              ov[u][0] = bf16_bits_to_float(h.x & 0xFFFFu); ov[u][1] = bf16_bits_to_float(h.x >> 16);
+              ov[u][2] = bf16_bits_to_float(h.y & 0xFFFFu); ov[u][3] = bf16_bits_to_float(h.y >> 16);
+            } else {
+              const uint32_t h = in ? __ldg(reinterpret_cast<const unsigned int*>(op)) : 0u;
+              ov[u][0] = bf16_bits_to_float(h & 0xFFFFu); ov[u][1] = bf16_bits_to_float(h >> 16);
+            }
+          } else {
+            const float* op = static_cast<const float*>(o) + base;
+            if constexpr (CW == 4) {
+              const float4 f = in ? __ldg(reinterpret_cast<const float4*>(op)) : make_float4(0.f, 0.f, 0.f, 0.f);
+              ov[u][0] = f.x; ov[u][1] = f.y; ov[u][2] = f.z; ov[u][3] = f.w;
+            } else {
+              const float2 f = in ? __ldg(reinterpret_cast<const float2*>(op)) : make_float2(0.f, 0.f);
+              ov[u][0] = f.x; ov[u][1] = f.y;
+            }
+          }
+          if constexpr (CW == 4) {
+            const uint2 h = in ? __ldg(reinterpret_cast<const uint2*>(dout + base)) : make_uint2(0u, 0u);
+            dh[u][0] = h.x;
+            dh[u][1] = h.y;
+          } else {
+            dh[u][0] = in ? __ldg(reinterpret_cast<const unsigned int*>(dout + base)) : 0u;
+          }
+        }
+        float part[kRowsPerStep];
+#pragma unroll
+        for (int u = 0; u < kRowsPerStep; ++u) {
+          part[u] = 0.f;
+#pragma unroll
+          for (int c = 0; c < CW / 2; ++c) {
+            part[u] = fmaf(ov[u][2 * c], bf16_bits_to_float(dh[u][c] & 0xFFFFu), part[u]);
+            part[u] = fmaf(ov[u][2 * c + 1], bf16_bits_to_float(dh[u][c] >> 16), part[u]);
+          }
+        }
+        // sum over the lanes, 16 rows at once: after the butterfly every lane
+        // holds all 16 totals, and lane l < 16 stores row r0 + l
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+          for (int u = 0; u < kRowsPerStep; ++u) part[u] += __shfl_xor_sync(0xffffffffu, part[u], off);
+        }
+        float mine = part[0];
+#pragma unroll
+        for (int u = 1; u < kRowsPerStep; ++u) mine = ((lane & 15) == u) ? part[u] : mine;
+        if (lane < kRowsPerStep) slot[r0 + lane] = mine;
+      }
+      mbar_arrive_warp(BAR(L::DD_FULL + (ddn & 1)));
+      ++ddn;
+    }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -1000,12 +1055,7 @@ template <int D, bool CAUSAL>
 cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
   if (stage == 0) {
-    if (a.o_bf16)
-      preprocess_kernel<D, true><<<a.grid_pre, 256, 0, stream>>>(a.o, a.dout, a.delta, a.heads * a.geom.nq);
-    else
-      preprocess_kernel<D, false><<<a.grid_pre, 256, 0, stream>>>(a.o, a.dout, a.delta, a.heads * a.geom.nq);
-  } else if (stage == 1) {
-    // dQ first: it turns D' = rowsum(dO o O) into the exact row term
+    // dQ first: it forms D' = rowsum(dO o O) and turns it into the exact row term
     using L = QLayout<D>;
     auto kern = dq_kernel<D, CAUSAL>;
     cudaFuncAttributes fattr;
@@ -1014,9 +1064,9 @@ cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
     if (fattr.numRegs != kKvLaunchRegs) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<a.grid_q, kQThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dq,
-                                                         a.geom, a.scale, a.scale_log2, a.sched_q, a.status,
-                                                         a.wait_limit_ns);
+    kern<<<a.grid_q, kQThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.o, a.dout,
+                                                         a.o_bf16, a.delta, a.dq, a.geom, a.scale, a.scale_log2,
+                                                         a.sched_q, a.status, a.wait_limit_ns);
   } else {
     using L = KvLayout<D>;
     auto kern = dkdv_kernel<D, CAUSAL>;
@@ -1036,7 +1086,7 @@ cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
 
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
-  for (int stage = 0; stage < 3; ++stage) {
+  for (int stage = 0; stage < 2; ++stage) {
     const cudaError_t e = launch_stage_t<D, CAUSAL>(a, stage, stream);
     if (e != cudaSuccess) return e;
   }

@@ -54,7 +54,6 @@ struct BwdArgs {
   float scale_log2;
   int grid_kv;                          // CTAs of the dK/dV kernel
   int grid_q;                           // CTAs of the dQ kernel
-  int grid_pre;                         // CTAs of the preprocess kernel
   SchedParams sched_kv;
   SchedParams sched_q;
   int* status;
@@ -82,8 +81,8 @@ struct DecArgs {
 
 cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);
 
-// The three stages of launch_bwd, for callers that time or order them
-// separately: 0 = preprocess (D'), 1 = dQ (corrects D), 2 = dK/dV.
+// The two stages of launch_bwd, for callers that time or order them
+// separately: 0 = dQ (forms the row term D), 1 = dK/dV.
 cudaError_t launch_bwd_stage(const BwdArgs& a, int stage, cudaStream_t stream);
 
 }  // namespace fa

@@ -168,8 +168,8 @@ size_t fa_fwd_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d);
  *   o, lse      : fp32 outputs of fa_fwd for the same q, k, v, scale, causal.
  *   dq, dk, dv  : fp32 [B][H][N][d], overwritten with dL/dQ, dL/dK, dL/dV.
  *   workspace   : fp32 buffer of fa_bwd_workspace_bytes(B, H, N) bytes that
- *                 receives the row term D_i = sum_j P_ij dP_ij (first as
- *                 rowsum(dO o O), then corrected to the probabilities the
+ *                 receives the row term D_i = sum_j P_ij dP_ij (formed from
+ *                 rowsum(dO o O) and corrected to the probabilities the
  *                 backward pass recomputes); or NULL, in which case the
  *                 library takes a stream-ordered allocation and frees it on
  *                 the same stream.
@@ -246,14 +246,13 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const floa
                          int causal, fa_stream_t stream);
 
 /*
- * One stage of fa_bwd, for callers that time or schedule the three kernels
- * separately; running stages 0, 1, 2 in order on one stream is exactly
- * fa_bwd with a caller-owned workspace (here required, never NULL).
- *   stage 0: D'_i = sum_c dO_ic O_ic into the workspace (reads o, dO only).
- *   stage 1: dQ; also rewrites the workspace with the exact row term
- *            D_i = sum_j P_ij dP_ij (needs stage 0 first).
- *   stage 2: dK and dV (needs stage 1 first).
- * Arguments as fa_bwd; a stage outside 0..2 returns FA_ERR_INVALID_ARG.
+ * One stage of fa_bwd, for callers that time or schedule the two kernels
+ * separately; running stages 0, 1 in order on one stream is exactly fa_bwd
+ * with a caller-owned workspace (here required, never NULL).
+ *   stage 0: dQ; also writes the exact row term D_i = sum_j P_ij dP_ij into
+ *            the workspace (formed from rowsum(dO o O) inside the kernel).
+ *   stage 1: dK and dV (needs stage 0 first).
+ * Arguments as fa_bwd; a stage outside 0..1 returns FA_ERR_INVALID_ARG.
  */
 fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const float* o, const float* lse,
                        const void* dO, float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d,
