@@ -272,7 +272,7 @@ def run_ours(args):
         if record:
             e[1].record(stream)
         if do_bwd:
-            # fa_bwd's three kernels, one C call each so each can be timed
+            # fa_bwd's two kernels, one C call each so each can be timed
             for stage in range(2):
                 fa.backward_stage(stage, q, k, v, o, lse, dout, dq, dk, dv, ws, causal=w.causal, scale=w.scale)
                 if record:

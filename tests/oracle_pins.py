@@ -140,8 +140,8 @@ def check_causal_is_prefix(ora):
 
 
 def check_backward_row_identity(ora):
-    """sum_j P_ij dP_ij equals rowsum(dO * O) (the identity the preprocess
-    kernel uses), to fp64 rounding."""
+    """sum_j P_ij dP_ij equals rowsum(dO * O) (the identity the backward's
+    row term starts from), to fp64 rounding."""
     q, k, v, do = _random_case(1, 2, 23, 8, 51)
     for causal in (False, True):
         o, _ = ora.forward(q, k, v, 0.4, causal)
