@@ -185,3 +185,28 @@ def test_square_call_equals_fa_bwd():
         fa.sync_status()
         for x, y in zip(a, b):
             assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+def test_padded_batch_longer_sequences(d, causal):
+    """A padded batch of multi-tile sequences (lengths not multiples of 128,
+    more keys than queries and the reverse), forward and backward, every
+    head against the oracle."""
+    B, H, Nq, Nk = 3, 2, 1500, 2100
+    sq, sk = [1500, 901, 1279], [2100, 1800, 640]
+    g = workloads.make_decode_inputs(B, H, Nq, Nk, d, seed=90 + d)
+    do = workloads.randn_bf16((B, H, Nq, d), 93 + d)
+    scale = scale_for(d)
+    q, k, v, doc = g["q"].cuda(), g["k"].cuda(), g["v"].cuda(), do.cuda()
+    lq = torch.tensor(sq, dtype=torch.int32, device="cuda")
+    lk = torch.tensor(sk, dtype=torch.int32, device="cuda")
+    o, lse = fa.forward_varlen(q, k, v, lq, lk, causal=causal, scale=scale)
+    ws = torch.empty(B * H * Nq, dtype=torch.float32, device="cuda")
+    got = fa.backward_varlen(q, k, v, o, lse, doc, lq, lk, causal=causal, scale=scale, workspace=ws)
+    fa.sync_status()
+    x = {n: to64(g[n]) for n in g}
+    o_ref, lse_ref = oracle.forward_varlen(x["q"], x["k"], x["v"], scale, causal, sq, sk)
+    _check(o, lse, o_ref, lse_ref, ("long padded", d, causal))
+    rq, rk, rv, rd = oracle.backward_varlen(x["q"], x["k"], x["v"], to64(do), scale, causal, sq, sk)
+    _check_grads(got, (rq, rk, rv), ("long padded", d, causal))
+    _check_delta(ws, rd, to64(do), ("long padded", d, causal))
