@@ -88,10 +88,11 @@ unsigned long long wait_limit_ns() {
   return v;
 }
 
-// Testing only: FA_TEST_STALL_UNIT=n makes CTA 0 of the next forward launches
-// skip one K tile of the n-th work unit it processes, so that a pipeline wait
-// runs out and the timeout path can be exercised without faulting anything.
-// Read on every call; unset (the default) means never.
+// Testing only: FA_TEST_STALL_UNIT=n makes CTA 0 of the next launches skip one
+// tile load of the n-th work unit it processes (the decode kernel: CTA n skips
+// its first stage), so that a pipeline wait runs out and the timeout path can
+// be exercised without faulting anything.  Read on every call; unset (the
+// default) means never.
 int test_stall_unit() {
   const char* s = std::getenv("FA_TEST_STALL_UNIT");
   return (s && *s) ? std::atoi(s) : -1;
@@ -214,6 +215,7 @@ fa_status bwd_prepare(fa::BwdArgs& a, const void* q, const void* k, const void* 
   a.grid_q = a.sched_q.grid;
   a.status = di.status;
   a.wait_limit_ns = wait_limit_ns();
+  a.stall_unit = test_stall_unit();
   return FA_OK;
 }
 
@@ -299,6 +301,7 @@ fa_status fa_fwd_decode(const void* q, const void* k, const void* v, float* o, f
   decode_splits(heads, Nk, di.sms, a.splits, a.chunk);
   a.status = di.status;
   a.wait_limit_ns = wait_limit_ns();
+  a.stall_unit = test_stall_unit();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float* part = workspace;
   if (a.splits > 1 && !part) {

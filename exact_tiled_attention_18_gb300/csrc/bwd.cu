@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const float* __restrict__ lse, const float* __restrict__ delta, float* __restrict__ dk,
                 float* __restrict__ dv, const SeqGeom geom, const float scale, const float scale_log2,
-                const SchedParams sp, int* status, const unsigned long long limit_ns) {
+                const SchedParams sp, int* status, const unsigned long long limit_ns, const int stall_unit) {
   using L = KvLayout<D>;
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -379,6 +379,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           const uint32_t s = qdpos % S, use = qdpos / S;
           ok = wait_bounded(BAR(L::QD_EMPTY + s), (use & 1) ^ 1, wc, SITE_KV_LOAD_QD, unit);
           if (!ok) break;
+          if (blockIdx.x == 0 && static_cast<int>(kvn) - 1 == stall_unit && i == i0) {
+            // testing hook: leave this (Q, dO) stage unloaded so the waits on
+            // it run out and the kernel reports a timeout instead of hanging
+            ++qdpos;
+            continue;
+          }
           mbar_arrive_expect_tx(BAR(L::QD_FULL + s), 2 * L::kTileBytes);
           const uint32_t qa = sbase + L::kQdOff + s * 2 * L::kTileBytes;
 #pragma unroll
@@ -590,7 +596,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
               const float* __restrict__ lse, const void* __restrict__ o, const uint16_t* __restrict__ dout,
               const int o_bf16, float* __restrict__ delta, float* __restrict__ dq, const SeqGeom geom,
               const float scale, const float scale_log2, const SchedParams sp, int* status,
-              const unsigned long long limit_ns) {
+              const unsigned long long limit_ns, const int stall_unit) {
   using L = QLayout<D>;
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -841,6 +847,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
           const uint32_t s = kvpos % S, use = kvpos / S;
           ok = wait_bounded(BAR(L::KV_EMPTY + s), (use & 1) ^ 1, wc, SITE_Q_LOAD_KV, unit);
           if (!ok) break;
+          if (blockIdx.x == 0 && static_cast<int>(qn) - 1 == stall_unit && jt == 0) {
+            // testing hook: leave this (K, V) stage unloaded (see dK/dV)
+            ++kvpos;
+            continue;
+          }
           mbar_arrive_expect_tx(BAR(L::KV_FULL + s), 2 * L::kTileBytes);
           const uint32_t ka = sbase + L::kKvOff + s * 2 * L::kTileBytes;
 #pragma unroll
@@ -1066,7 +1077,7 @@ cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     kern<<<a.grid_q, kQThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.o, a.dout,
                                                          a.o_bf16, a.delta, a.dq, a.geom, a.scale, a.scale_log2,
-                                                         a.sched_q, a.status, a.wait_limit_ns);
+                                                         a.sched_q, a.status, a.wait_limit_ns, a.stall_unit);
   } else {
     using L = KvLayout<D>;
     auto kern = dkdv_kernel<D, CAUSAL>;
@@ -1079,7 +1090,7 @@ cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     kern<<<a.grid_kv, kKvThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dk,
                                                            a.dv, a.geom, a.scale, a.scale_log2, a.sched_kv, a.status,
-                                                           a.wait_limit_ns);
+                                                           a.wait_limit_ns, a.stall_unit);
   }
   return cudaGetLastError();
 }

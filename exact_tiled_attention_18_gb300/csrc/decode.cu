@@ -74,7 +74,8 @@ __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NQ>())
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const uint16_t* __restrict__ q, float* __restrict__ o, float* __restrict__ lse,
                   float* __restrict__ part, const SeqGeom geom, const float scale_log2, const int causal,
-                  const int splits, const int chunk, int* status, const unsigned long long limit_ns) {
+                  const int splits, const int chunk, int* status, const unsigned long long limit_ns,
+                  const int stall_unit) {
   using L = DecLayout<D, NQ>;
   constexpr int S = L::kStages;
   constexpr int G = D / 16;        // lanes per key in the score phase, 16 columns each
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_ctas_per_sm<NQ>())
         const int s = issued % S;
         ok = wait_bounded(bars + 8 * (S + s), ((issued / S) & 1) ^ 1, wc, SITE_DEC_EMPTY, unit);
         if (!ok) break;
+        if (unit == stall_unit && issued == 0) continue;  // testing hook: leave this stage unloaded
         const uint32_t full = bars + 8 * s;
         mbar_arrive_expect_tx(full, L::kStage);
         const uint32_t st = sbase + s * L::kStage;
@@ -373,7 +375,7 @@ cudaError_t launch_decode_t(const DecArgs& a, cudaStream_t stream) {
   const long long grid = static_cast<long long>(a.heads) * a.splits;
   kern<<<static_cast<unsigned>(grid), kDecThreads, L::kSmemBytes, stream>>>(
       a.tm_k, a.tm_v, a.q, a.o, a.lse, a.part, a.geom, a.scale_log2, a.causal, a.splits, a.chunk, a.status,
-      a.wait_limit_ns);
+      a.wait_limit_ns, a.stall_unit);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
   const int rows = a.heads * a.geom.nq;

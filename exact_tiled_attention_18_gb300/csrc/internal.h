@@ -58,6 +58,7 @@ struct BwdArgs {
   SchedParams sched_q;
   int* status;
   unsigned long long wait_limit_ns;
+  int stall_unit;                       // testing: CTA 0 skips one stage of its n-th unit (-1: never)
 };
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
@@ -77,6 +78,7 @@ struct DecArgs {
   int chunk;               // keys per split, a multiple of 64
   int* status;
   unsigned long long wait_limit_ns;
+  int stall_unit;          // testing: CTA n leaves its first stage unloaded (-1: never)
 };
 
 cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);

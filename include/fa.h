@@ -41,8 +41,9 @@
  *    kernels is bounded (4 s by default; the FA_WAIT_LIMIT_MS environment
  *    variable, read once per process, changes it), so a failing kernel
  *    returns instead of hanging.  For tests of that path only,
- *    FA_TEST_STALL_UNIT=n (read on every fa_fwd call) makes the first CTA
- *    leave one K tile of its n-th work unit unloaded: its waits run out and
+ *    FA_TEST_STALL_UNIT=n (read on every call that launches work) makes the
+ *    first CTA leave one tile of its n-th work unit unloaded (fa_fwd_decode:
+ *    CTA n leaves its first stage unloaded): its waits run out and
  *    fa_sync_status() then reports FA_ERR_TIMEOUT.
  *  - Thread safety: calls may be made from several host threads; calls on
  *    different devices are independent.
