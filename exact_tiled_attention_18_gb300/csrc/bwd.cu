@@ -411,6 +411,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
+      // Descriptors built once; a stage or K step only moves the start-address
+      // field (16-byte units), a plain add.  K-major views feed S^T and dP^T,
+      // MN-major views (next 64-column block 16 KB away) feed dV and dK.
+      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+      const uint64_t kdesc = sdesc_sw128(sbase + L::kKOff, 16, 1024);
+      const uint64_t vdesc = sdesc_sw128(sbase + L::kVOff, 16, 1024);
+      const uint64_t qd_k0 = sdesc_sw128(sbase + L::kQdOff, 16, 1024);
+      const uint64_t qd_mn0 = sdesc_sw128(sbase + L::kQdOff, kTileRows * 128, 1024);
+      auto q_k = [&](uint32_t pos) { return qd_k0 + static_cast<uint64_t>(pos % S) * (2 * kTileUnits); };
+      auto q_mn = [&](uint32_t pos) { return qd_mn0 + static_cast<uint64_t>(pos % S) * (2 * kTileUnits); };
       uint32_t kvn = 0, qdpos = 0, pn = 0;
       SchedIter it = sched_begin(sp);
       int head, j;
@@ -425,30 +435,27 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         ++kvn;
         // S^T = K Q^T and dP^T = V dO^T of one query tile: M = 128 keys,
         // N = 128 queries, K = d
-        auto issue_s = [&](uint32_t qa) {
+        auto issue_s = [&](uint64_t qd) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            umma_ss(tmem + L::kColS, sdesc_sw128(sbase + L::kKOff + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
-                    id_s, ks > 0 ? 1u : 0u);
+            const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            umma_ss(tmem + L::kColS, kdesc + off, qd + off, id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::S_FULL));
         };
-        auto issue_dp = [&](uint32_t da) {
+        auto issue_dp = [&](uint64_t dd) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            umma_ss(tmem + L::kColDP, sdesc_sw128(sbase + L::kVOff + off, 16, 1024),
-                    sdesc_sw128(da + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+            const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            umma_ss(tmem + L::kColDP, vdesc + off, dd + off, id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::DP_FULL));
         };
-        auto stage_addr = [&](uint32_t pos) { return sbase + L::kQdOff + (pos % S) * 2 * L::kTileBytes; };
         ok = wait_bounded(BAR(L::QD_FULL + qdpos % S), (qdpos / S) & 1, wc, SITE_KV_MMA_QD, unit);
         if (!ok) break;
         tc_fence_after();
-        issue_s(stage_addr(qdpos));
-        issue_dp(stage_addr(qdpos) + L::kTileBytes);
+        issue_s(q_k(qdpos));
+        issue_dp(q_k(qdpos) + kTileUnits);
         // Per query tile i: dV += P^T dO once P^T is stored; then S^T of tile
         // i+1, which overwrites P^T(i) only after dV(i) has read it (the
         // tensor pipe runs in issue order), so the elementwise warps find
@@ -459,8 +466,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         // [64 w, 64 w + 32) and [64 w + 32, 64 w + 64).
         for (int i = i0; i < i1; ++i) {
           const uint32_t s = qdpos % S;
-          const uint32_t qa = stage_addr(qdpos);
-          const uint32_t da = qa + L::kTileBytes;
+          const uint64_t qmn = q_mn(qdpos);
+          const uint64_t dmn = qmn + kTileUnits;
           ok = wait_bounded(BAR(L::P_READY), pn & 1, wc, SITE_KV_MMA_PDS, unit);
           if (!ok) break;
           tc_fence_after();
@@ -468,15 +475,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDV, tmem + L::kColS + acol, sdesc_sw128(da + ks * 2048, kTileRows * 128, 1024),
-                    id_acc, (!first || ks > 0) ? 1u : 0u);
+            umma_ts(tmem + L::kColDV, tmem + L::kColS + acol, dmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
+                    (!first || ks > 0) ? 1u : 0u);
           }
           const bool more = i + 1 < i1;
           if (more) {
             ok = wait_bounded(BAR(L::QD_FULL + (qdpos + 1) % S), ((qdpos + 1) / S) & 1, wc, SITE_KV_MMA_QD, unit);
             if (!ok) break;
             tc_fence_after();
-            issue_s(stage_addr(qdpos + 1));
+            issue_s(q_k(qdpos + 1));
           }
           ok = wait_bounded(BAR(L::DS_READY), pn & 1, wc, SITE_KV_MMA_PDS, unit);
           if (!ok) break;
@@ -485,18 +492,18 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDK, tmem + L::kColDP + acol, sdesc_sw128(qa + ks * 2048, kTileRows * 128, 1024),
-                    id_acc, (!first || ks > 0) ? 1u : 0u);
+            umma_ts(tmem + L::kColDK, tmem + L::kColDP + acol, qmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
+                    (!first || ks > 0) ? 1u : 0u);
           }
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {  // dS^T lo part
             const uint32_t acol = 32 + 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDK, tmem + L::kColDP + acol, sdesc_sw128(qa + ks * 2048, kTileRows * 128, 1024),
-                    id_acc, 1u);
+            umma_ts(tmem + L::kColDK, tmem + L::kColDP + acol, qmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
+                    1u);
           }
           umma_commit(BAR(L::QD_EMPTY + s));
           ++qdpos;
-          if (more) issue_dp(stage_addr(qdpos) + L::kTileBytes);
+          if (more) issue_dp(q_k(qdpos) + kTileUnits);
         }
         if (!ok) break;
         umma_commit(BAR(L::ACC_FULL));
@@ -960,6 +967,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
+      // Descriptors built once (see the dK/dV kernel): Q and dO K-major for
+      // S and dP; the K/V stages K-major for S and dP, K MN-major for dQ and B.
+      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+      const uint64_t qdesc = sdesc_sw128(sbase + L::kQOff, 16, 1024);
+      const uint64_t dodesc = sdesc_sw128(sbase + L::kDoOff, 16, 1024);
+      const uint64_t kv_k0 = sdesc_sw128(sbase + L::kKvOff, 16, 1024);
+      const uint64_t kv_mn0 = sdesc_sw128(sbase + L::kKvOff, kTileRows * 128, 1024);
+      auto kv_k = [&](uint32_t pos) { return kv_k0 + static_cast<uint64_t>(pos % S) * (2 * kTileUnits); };
+      auto kv_mn = [&](uint32_t pos) { return kv_mn0 + static_cast<uint64_t>(pos % S) * (2 * kTileUnits); };
       uint32_t qn = 0, kvpos = 0, dn = 0;
       SchedIter it = sched_begin(sp);
       int head, i;
@@ -973,30 +989,27 @@ __global__ void __launch_bounds__(kQThreads, 1)
         ++qn;
         // S = Q K^T and dP = dO V^T of one key tile: M = 128 queries,
         // N = 128 keys, K = d
-        auto issue_s = [&](uint32_t ka) {
+        auto issue_s = [&](uint64_t kd) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            umma_ss(tmem + L::kColS, sdesc_sw128(sbase + L::kQOff + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                    id_s, ks > 0 ? 1u : 0u);
+            const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            umma_ss(tmem + L::kColS, qdesc + off, kd + off, id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::S_FULL));
         };
-        auto issue_dp = [&](uint32_t va) {
+        auto issue_dp = [&](uint64_t vd) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            umma_ss(tmem + L::kColDP, sdesc_sw128(sbase + L::kDoOff + off, 16, 1024),
-                    sdesc_sw128(va + off, 16, 1024), id_s, ks > 0 ? 1u : 0u);
+            const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            umma_ss(tmem + L::kColDP, dodesc + off, vd + off, id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::DP_FULL));
         };
-        auto kv_addr = [&](uint32_t pos) { return sbase + L::kKvOff + (pos % S) * 2 * L::kTileBytes; };
         ok = wait_bounded(BAR(L::KV_FULL + kvpos % S), (kvpos / S) & 1, wc, SITE_Q_MMA_KV, unit);
         if (!ok) break;
         tc_fence_after();
-        issue_s(kv_addr(kvpos));
-        issue_dp(kv_addr(kvpos) + L::kTileBytes);
+        issue_s(kv_k(kvpos));
+        issue_dp(kv_k(kvpos) + kTileUnits);
         // Per key tile jt: B += P K once P is stored; then S of tile jt+1,
         // which overwrites P(jt) only after B(jt) has read it (the tensor
         // pipe runs in issue order); then dQ += dS K (hi and lo, both in the
@@ -1006,22 +1019,22 @@ __global__ void __launch_bounds__(kQThreads, 1)
         // [64 w, 64 w + 32) and [64 w + 32, 64 w + 64).
         for (int jt = 0; jt < nk; ++jt) {
           const uint32_t s = kvpos % S;
-          const uint32_t ka = kv_addr(kvpos);
+          const uint64_t kmn = kv_mn(kvpos);
           ok = wait_bounded(BAR(L::P_READY), dn & 1, wc, SITE_Q_MMA_P, unit);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {  // B += P K, for the delta correction
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColB, tmem + L::kColS + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
-                    id_acc, (jt > 0 || ks > 0) ? 1u : 0u);
+            umma_ts(tmem + L::kColB, tmem + L::kColS + acol, kmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
+                    (jt > 0 || ks > 0) ? 1u : 0u);
           }
           const bool more = jt + 1 < nk;
           if (more) {
             ok = wait_bounded(BAR(L::KV_FULL + (kvpos + 1) % S), ((kvpos + 1) / S) & 1, wc, SITE_Q_MMA_KV, unit);
             if (!ok) break;
             tc_fence_after();
-            issue_s(kv_addr(kvpos + 1));
+            issue_s(kv_k(kvpos + 1));
           }
           ok = wait_bounded(BAR(L::DS_FULL), dn & 1, wc, SITE_Q_MMA_DS, unit);
           if (!ok) break;
@@ -1030,18 +1043,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDQ, tmem + L::kColDP + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
-                    id_acc, (jt > 0 || ks > 0) ? 1u : 0u);
+            umma_ts(tmem + L::kColDQ, tmem + L::kColDP + acol, kmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
+                    (jt > 0 || ks > 0) ? 1u : 0u);
           }
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {  // dS lo part
             const uint32_t acol = 32 + 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDQ, tmem + L::kColDP + acol, sdesc_sw128(ka + ks * 2048, kTileRows * 128, 1024),
-                    id_acc, 1u);
+            umma_ts(tmem + L::kColDQ, tmem + L::kColDP + acol, kmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
+                    1u);
           }
           umma_commit(BAR(L::KV_EMPTY + s));
           ++kvpos;
-          if (more) issue_dp(kv_addr(kvpos) + L::kTileBytes);
+          if (more) issue_dp(kv_k(kvpos) + kTileUnits);
         }
         if (!ok) break;
         umma_commit(BAR(L::ACC_FULL));
