@@ -501,9 +501,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           umma_commit(BAR(L::KV_EMPTY + vpos % S));  // V_j is free once PV(j) of both tiles completes
           if (next_b) {
-            ok = wait_bounded(BAR(L::KV_FULL + knext % S), (knext / S) & 1, wc, SITE_MMA_KV, unit);
-            if (!ok) break;
-            tc_fence_after();
+            if (!(has_a && next_a)) {  // otherwise tile A's S(j+1) already waited for K_{j+1}
+              ok = wait_bounded(BAR(L::KV_FULL + knext % S), (knext / S) & 1, wc, SITE_MMA_KV, unit);
+              if (!ok) break;
+              tc_fence_after();
+            }
             issue_s(1, slot_addr(knext));
             umma_commit(BAR(L::S_FULL + 1));
           }
