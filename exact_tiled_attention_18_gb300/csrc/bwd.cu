@@ -44,7 +44,7 @@ enum BwdSite : int {
   SITE_KV_MMA_QD = 15,
   SITE_KV_MMA_PDS = 16,
   SITE_KV_EW_LD = 17,
-  SITE_KV_EW_SDP = 18,
+  SITE_KV_EW_S = 18,
   SITE_KV_EW_ACC = 19,
   SITE_KV_EW_DP = 20,
   SITE_Q_LOAD_Q = 21,
@@ -52,7 +52,7 @@ enum BwdSite : int {
   SITE_Q_MMA_Q = 23,
   SITE_Q_MMA_KV = 24,
   SITE_Q_MMA_DS = 25,
-  SITE_Q_EW_SDP = 26,
+  SITE_Q_EW_S = 26,
   SITE_Q_EW_ACC = 27,
   SITE_Q_EW_XCH = 28,
   SITE_Q_EW_DP = 29,
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (!ok) break;
         // P^T needs only S^T: dP^T may still be in the tensor pipe
         const uint32_t sdp_parity = sn & 1;
-        ok = warp_wait(BAR(L::S_FULL), sdp_parity, wc, SITE_KV_EW_SDP, unit);
+        ok = warp_wait(BAR(L::S_FULL), sdp_parity, wc, SITE_KV_EW_S, unit);
         if (!ok) break;
         ++sn;
         tc_fence_after();
@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // ------------------------------------------------- dS (thread = query row)
     regs_increase<kKvEwRegs>();
     // The row term comes in as D'_i = rowsum(dO o O) (computed by the loader
-    // warp one unit ahead) with O from the forward pass, whose P was rounded
+    // warps one unit ahead) with O from the forward pass, whose P was rounded
     // to bf16 for the PV product.  The kernel sees every key of its rows, so
     // it also sums delta_i = sum_j dS'_ij = sum_j P_ij dP_ij - D'_i in fp32,
     // corrects its own product with
@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       for (int jt = 0; jt < nk; ++jt) {
         // P needs only S: dP may still be in the tensor pipe
         const uint32_t sdp_parity = sn & 1;
-        ok = warp_wait(BAR(L::S_FULL), sdp_parity, wc, SITE_Q_EW_SDP, unit);
+        ok = warp_wait(BAR(L::S_FULL), sdp_parity, wc, SITE_Q_EW_S, unit);
         if (!ok) break;
         ++sn;
         tc_fence_after();
