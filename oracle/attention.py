@@ -36,6 +36,10 @@ Readings where the pages are silent (each is also a test pin or an argument):
   sees every key; if Nq > Nk the first Nq - Nk queries see none;
 * padded batches carry a valid length per sequence; rows past it are padding
   and are defined as O = 0, LSE = -inf (gradients 0);
+* the "+ mask" of the definition, in general form, is an additive bias
+  B_ij on the scaled scores (s_ij = scale * q_i.k_j + B_ij), -inf entries
+  hiding a key; it combines with the causal rule, and a row whose keys are
+  all hidden is a fully masked row (O = 0, LSE = -inf);
 * the log-sum-exp is in natural-log units of the scaled scores:
   LSE_i = ln sum_j exp(s_ij) over eligible j;
 * ``scale`` is an argument (the pages' 1/sqrt(d) is the caller's default);
@@ -86,20 +90,24 @@ def eligible(nq: int, nk: int, causal: bool) -> np.ndarray:
     return j <= i + (nk - nq)
 
 
-def _masked_scores(q, k, scale, causal):
+def _masked_scores(q, k, scale, causal, bias=None):
     s = scores(q, k, scale)
     ok = eligible(q.shape[0], k.shape[0], causal)
+    if bias is not None:
+        s = s + bias
+        ok = ok & (bias > -np.inf)
     return np.where(ok, s, -np.inf), ok
 
 
-def forward_head(q, k, v, scale, causal):
-    """One head of softmax(scale * q k^T + mask) v.
+def forward_head(q, k, v, scale, causal, bias=None):
+    """One head of softmax(scale * q k^T + mask) v; ``bias`` ([Nq, Nk] or
+    None) is the additive mask, on top of the causal rule.
 
     Returns (O [N, d], LSE [N]) in float64.  The row maximum is subtracted
     before exponentiating only so that exp() cannot overflow; the result is
     the same number the definition gives (softmax is shift invariant).
     """
-    s, ok = _masked_scores(q, k, scale, causal)
+    s, ok = _masked_scores(q, k, scale, causal, bias)
     has_key = ok.any(axis=1)
     m = np.where(has_key, s.max(axis=1, initial=-np.inf), 0.0)
     w = np.where(ok, np.exp(s - m[:, None]), 0.0)  # unnormalised weights
@@ -111,24 +119,26 @@ def forward_head(q, k, v, scale, causal):
     return o, lse
 
 
-def forward(q, k, v, scale, causal):
-    """Attention over [B, H, N, d] arrays; returns (O [B,H,N,d], LSE [B,H,N])."""
+def forward(q, k, v, scale, causal, bias=None):
+    """Attention over [B, H, N, d] arrays; returns (O [B,H,N,d], LSE [B,H,N]).
+    ``bias``: None or [B, H, Nq, Nk] additive mask."""
     b, h, n, d = q.shape
     o = np.empty((b, h, n, v.shape[-1]), dtype=np.float64)
     lse = np.empty((b, h, n), dtype=np.float64)
     for bi in range(b):
         for hi in range(h):
-            o[bi, hi], lse[bi, hi] = forward_head(q[bi, hi], k[bi, hi], v[bi, hi], scale, causal)
+            o[bi, hi], lse[bi, hi] = forward_head(q[bi, hi], k[bi, hi], v[bi, hi], scale, causal,
+                                                  None if bias is None else bias[bi, hi])
     return o, lse
 
 
-def forward_rows(q, k, v, scale, causal, rows):
+def forward_rows(q, k, v, scale, causal, rows, bias=None):
     """O and LSE for selected query rows only.
 
     ``rows`` is a sequence of (b, h, i) triples.  Each row is the definition
     evaluated for that one query against every eligible key of its head, so a
     long sequence can be checked on a sample without the N x N matrix.
-    Returns (O [R, d], LSE [R]).
+    ``bias``: None or [B, H, Nq, Nk] additive mask.  Returns (O [R, d], LSE [R]).
     """
     out_o = np.empty((len(rows), v.shape[-1]), dtype=np.float64)
     out_l = np.empty(len(rows), dtype=np.float64)
@@ -142,18 +152,25 @@ def forward_rows(q, k, v, scale, causal, rows):
         kk = k[bi, hi, :count]
         vv = v[bi, hi, :count]
         s = scale * (kk @ q[bi, hi, i])
+        if bias is not None:
+            s = s + bias[bi, hi, i, :count]
+        if not np.any(s > -np.inf):
+            out_o[r] = 0.0
+            out_l[r] = -np.inf
+            continue
         m = s.max()
-        w = np.exp(s - m)
+        w = np.exp(s - m)  # hidden keys (s = -inf) give 0
         l = w.sum()
         out_o[r] = (w @ vv) / l
         out_l[r] = m + math.log(l)
     return out_o, out_l
 
 
-def forward_varlen(q, k, v, scale, causal, seqlens_q, seqlens_k):
+def forward_varlen(q, k, v, scale, causal, seqlens_q, seqlens_k, bias=None):
     """Padded batch: sequence b uses its first seqlens_q[b] query rows and
-    seqlens_k[b] key rows of q [B,H,Nq,d] and k, v [B,H,Nk,d].  Padding rows
-    are O = 0, LSE = -inf.  Returns (O [B,H,Nq,d], LSE [B,H,Nq])."""
+    seqlens_k[b] key rows of q [B,H,Nq,d] and k, v [B,H,Nk,d] (and the
+    matching corner of bias [B,H,Nq,Nk]).  Padding rows are O = 0,
+    LSE = -inf.  Returns (O [B,H,Nq,d], LSE [B,H,Nq])."""
     b, h, nq, _ = q.shape
     o = np.zeros((b, h, nq, v.shape[-1]), dtype=np.float64)
     lse = np.full((b, h, nq), -np.inf, dtype=np.float64)
@@ -161,7 +178,8 @@ def forward_varlen(q, k, v, scale, causal, seqlens_q, seqlens_k):
         lq, lk = int(seqlens_q[bi]), int(seqlens_k[bi])
         for hi in range(h):
             o[bi, hi, :lq], lse[bi, hi, :lq] = forward_head(q[bi, hi, :lq], k[bi, hi, :lk], v[bi, hi, :lk],
-                                                            scale, causal)
+                                                            scale, causal,
+                                                            None if bias is None else bias[bi, hi, :lq, :lk])
     return o, lse
 
 

@@ -163,10 +163,11 @@ def check_forward_rows_agree(ora):
 
 # ---------------------------------------------------------------- brute force
 
-def _mp_forward(q, k, v, scale, causal):
+def _mp_forward(q, k, v, scale, causal, bias=None):
     """Definition evaluated entry by entry in 50-digit arithmetic (one head).
     Causal keys of query i: 0 .. i + (nk - nq), the last query aligned with
-    the last key; a query with no key gets O = 0 and LSE = -inf."""
+    the last key; a query with no key gets O = 0 and LSE = -inf.  ``bias``
+    (finite, [nq][nk]) is added to each scaled score."""
     nq, nk, d, dv = len(q), len(k), len(q[0]), len(v[0])
     o = [[mpmath.mpf(0)] * dv for _ in range(nq)]
     lse = [mpmath.mpf("-inf")] * nq
@@ -179,7 +180,7 @@ def _mp_forward(q, k, v, scale, causal):
             s = mpmath.mpf(0)
             for c in range(d):
                 s += q[i][c] * k[j][c]
-            w[j] = mpmath.exp(scale * s)
+            w[j] = mpmath.exp(scale * s + (bias[i][j] if bias is not None else 0))
         tot = mpmath.fsum(w.values())
         lse[i] = mpmath.log(tot)
         for c in range(dv):
@@ -323,6 +324,93 @@ def check_memory_exercise(ora):
     assert ora.score_matrix_payload_bytes(64000, 1) == g["score_elements_64000_tokens"]
 
 
+# ---------------------------------------------------------------- additive mask
+
+def _bias_case(nq, nk, seed):
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((1, 2, nq, nk)) * 2.0
+
+
+def check_bias_zero_is_no_bias(ora):
+    """A zero additive mask changes nothing, bit for bit."""
+    q, k, v, _ = _random_case(1, 2, 11, 8, 61)
+    for causal in (False, True):
+        a = ora.forward(q, k, v, 0.3, causal)
+        b = ora.forward(q, k, v, 0.3, causal, np.zeros((1, 2, 11, 11)))
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def check_bias_row_constant(ora):
+    """A bias constant along each row cancels in the softmax: O is unchanged
+    and LSE_i moves by exactly that constant."""
+    q, k, v, _ = _random_case(1, 2, 9, 8, 62)
+    c = np.random.default_rng(7).standard_normal((1, 2, 9)) * 3.0
+    bias = np.broadcast_to(c[..., None], (1, 2, 9, 9)).copy()
+    for causal in (False, True):
+        o0, l0 = ora.forward(q, k, v, 0.4, causal)
+        o1, l1 = ora.forward(q, k, v, 0.4, causal, bias)
+        assert np.max(np.abs(o1 - o0)) < 1e-13
+        assert np.max(np.abs(l1 - (l0 + c))) < 1e-12
+
+
+def check_bias_masks_like_causal(ora):
+    """A bias of 0 on eligible keys and -inf elsewhere, without the causal
+    rule, is the causal rule (unequal lengths, bottom-right alignment)."""
+    rng = np.random.default_rng(63)
+    q = rng.standard_normal((1, 1, 6, 4))
+    k, v = rng.standard_normal((2, 1, 1, 9, 4))
+    i = np.arange(6)[:, None]
+    j = np.arange(9)[None, :]
+    bias = np.where(j <= i + 3, 0.0, -np.inf)[None, None]
+    a = ora.forward(q, k, v, 0.5, True)
+    b = ora.forward(q, k, v, 0.5, False, bias)
+    assert np.max(np.abs(a[0] - b[0])) < 1e-14 and np.max(np.abs(a[1] - b[1])) < 1e-14
+
+
+def check_bias_fully_hidden_row(ora):
+    """A row whose keys the mask hides entirely: O = 0, LSE = -inf, no NaN;
+    other rows as without that row's mask."""
+    q, k, v, _ = _random_case(1, 1, 5, 4, 64)
+    bias = np.zeros((1, 1, 5, 5))
+    bias[0, 0, 2, :] = -np.inf
+    o, lse = ora.forward(q, k, v, 0.5, False, bias)
+    assert np.all(o[0, 0, 2] == 0) and lse[0, 0, 2] == -np.inf and np.all(np.isfinite(o))
+    o0, l0 = ora.forward(q, k, v, 0.5, False)
+    keep = [0, 1, 3, 4]
+    assert np.max(np.abs(o[0, 0, keep] - o0[0, 0, keep])) < 1e-15
+
+
+def check_brute_force_bias(ora):
+    """Random bias on a 4-query x 6-key head, causal, against the definition
+    in 50-digit arithmetic."""
+    mpmath.mp.dps = 50
+    q = _bf16_values((4, 4), 71)
+    k, v = (_bf16_values((6, 4), 72 + t) for t in range(2))
+    bias = np.random.default_rng(73).standard_normal((4, 6)) * 1.5
+    scale = 0.5
+    o_ref, lse_ref = _mp_forward(_to_mp(q), _to_mp(k), _to_mp(v), mpmath.mpf(scale), True,
+                                 [[mpmath.mpf(float(x)) for x in row] for row in bias])
+    o, lse = ora.forward(_head(q), _head(k), _head(v), scale, True, bias[None, None])
+    o_ref = np.array([[float(x) for x in row] for row in o_ref])
+    lse_ref = np.array([float(x) for x in lse_ref])
+    assert np.max(np.abs(o[0, 0] - o_ref)) < 1e-13
+    assert np.max(np.abs(lse[0, 0] - lse_ref)) < 1e-13
+
+
+def check_forward_rows_with_bias(ora):
+    """The row sampler sees the same bias as the full forward."""
+    q, k, v, _ = _random_case(2, 2, 13, 8, 65)
+    bias = np.random.default_rng(66).standard_normal((2, 2, 13, 13))
+    bias[1, 0, 4, :3] = -np.inf
+    rows = [(0, 0, 0), (1, 0, 4), (1, 1, 12), (0, 1, 7)]
+    for causal in (False, True):
+        o, lse = ora.forward(q, k, v, 0.35, causal, bias)
+        ro, rl = ora.forward_rows(q, k, v, 0.35, causal, rows, bias)
+        for r, (b_, h_, i_) in enumerate(rows):
+            assert np.max(np.abs(ro[r] - o[b_, h_, i_])) < 1e-13
+            assert abs(rl[r] - lse[b_, h_, i_]) < 1e-13
+
+
 ALL_CHECKS = [
     check_two_tile_example,
     check_common_shift,
@@ -339,6 +427,12 @@ ALL_CHECKS = [
     check_leading_rows_masked,
     check_varlen_slices,
     check_memory_exercise,
+    check_bias_zero_is_no_bias,
+    check_bias_row_constant,
+    check_bias_masks_like_causal,
+    check_bias_fully_hidden_row,
+    check_brute_force_bias,
+    check_forward_rows_with_bias,
 ]
 
 

@@ -28,6 +28,11 @@ MUTATIONS = {
     "rows_off_by_one": ("count = min(i + (nk_all - nq) + 1, nk_all)", "count = min(i + (nk_all - nq), nk_all)"),
     "causal_offset_flipped": ("return j <= i + (nk - nq)", "return j <= i - (nk - nq)"),
     "causal_top_left": ("return j <= i + (nk - nq)", "return j <= i"),
+    "bias_ignored": ("        s = s + bias\n        ok = ok & (bias > -np.inf)", "        ok = ok & (bias > -np.inf)"),
+    "bias_scaled_with_scores": ("        s = s + bias\n        ok", "        s = s + scale * bias\n        ok"),
+    "bias_transposed": ("        s = s + bias\n        ok", "        s = s + bias.T\n        ok"),
+    "bias_sign_flipped": ("        s = s + bias\n        ok", "        s = s - bias\n        ok"),
+    "rows_bias_ignored": ("            s = s + bias[bi, hi, i, :count]", "            s = s + 0.0"),
     "varlen_keys_sliced_by_query_length": ("v[bi, hi, :lk],\n                                                            scale", "v[bi, hi, :lq],\n                                                            scale"),
 }
 
