@@ -47,12 +47,15 @@ def lib() -> ctypes.CDLL:
                 f"{LIB_PATH} is missing: build it with `python -m exact_tiled_attention_18_gb300.build`")
         L = ctypes.CDLL(LIB_PATH)
         vp, i, f, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int
+        ll = ctypes.c_longlong
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_fwd.restype = st
         L.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_fwd_varlen.restype = st
         L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_fwd_ex.restype = st
+        L.fa_fwd_bias.argtypes = [vp, vp, vp, vp, i, vp, vp, ll, ll, ll, vp, vp, i, i, i, i, i, f, i, vp]
+        L.fa_fwd_bias.restype = st
         L.fa_bwd_ex.argtypes = [vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_bwd_ex.restype = st
         L.fa_fwd_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
@@ -75,7 +78,6 @@ def lib() -> ctypes.CDLL:
         L.fa_last_failure.restype = st
         L.fa_status_string.argtypes = [st]
         L.fa_status_string.restype = ctypes.c_char_p
-        ll = ctypes.c_longlong
         ip = ctypes.POINTER(ctypes.c_int)
         L.fa_sched_enumerate.argtypes = [i, i, i, i, i, ll, ip, ip, ip, ll]
         L.fa_sched_enumerate.restype = ll
@@ -106,6 +108,13 @@ def fa_fwd_varlen(q: int, k: int, v: int, o: int, lse: int, seqlens_q: int, seql
 def fa_fwd_ex(q: int, k: int, v: int, o: int, o_dtype: int, lse: int, seqlens_q: int, seqlens_k: int, B: int,
               H: int, Nq: int, Nk: int, d: int, scale: float, causal: int, stream: int) -> int:
     return lib().fa_fwd_ex(q, k, v, o, o_dtype, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream)
+
+
+def fa_fwd_bias(q: int, k: int, v: int, o: int, o_dtype: int, lse: int, bias: int, bias_stride_b: int,
+                bias_stride_h: int, bias_stride_q: int, seqlens_q: int, seqlens_k: int, B: int, H: int, Nq: int,
+                Nk: int, d: int, scale: float, causal: int, stream: int) -> int:
+    return lib().fa_fwd_bias(q, k, v, o, o_dtype, lse, bias, bias_stride_b, bias_stride_h, bias_stride_q, seqlens_q,
+                             seqlens_k, B, H, Nq, Nk, d, scale, causal, stream)
 
 
 def fa_bwd_ex(q: int, k: int, v: int, o: int, o_dtype: int, lse: int, do: int, dq: int, dk: int, dv: int,
@@ -252,6 +261,47 @@ def forward_varlen(q, k, v, seqlens_q=None, seqlens_k=None, causal: bool = False
                                       _stream_handle(q.device)))
     else:
         raise ValueError("O must be float32 or bfloat16")
+    return o, lse
+
+
+def forward_bias(q, k, v, bias, seqlens_q=None, seqlens_k=None, causal: bool = False, scale: float | None = None,
+                 o_dtype=None, out=None):
+    """O, LSE through fa_fwd_bias: softmax(scale * q k^T + bias) v.  ``bias``
+    is a bf16 CUDA tensor broadcastable to [B, H, Nq, Nk] (e.g. made with
+    expand()) whose last dimension is contiguous; other arguments as
+    forward_varlen."""
+    import torch
+    for t in (q, k, v):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v must be contiguous 4-D bf16 CUDA tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, H, Nk, d] with the batch, heads and d of q")
+    if not bias.is_cuda or bias.dtype != torch.bfloat16:
+        raise ValueError("bias must be a bf16 CUDA tensor")
+    bias = bias.expand(B, H, Nq, Nk)
+    if bias.stride(3) != 1:
+        raise ValueError("the bias's key dimension must be contiguous")
+    for t in (seqlens_q, seqlens_k):
+        if t is not None and (not t.is_cuda or t.dtype != torch.int32 or t.numel() != B or not t.is_contiguous()):
+            raise ValueError("seqlens must be contiguous int32 CUDA tensors of B entries")
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    if out is None:
+        o = torch.empty((B, H, Nq, d), dtype=o_dtype or torch.float32, device=q.device)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    if o.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("O must be float32 or bfloat16")
+    sb, sh, sq, _ = bias.stride()
+    _check("fa_fwd_bias", fa_fwd_bias(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      FA_DTYPE_BF16 if o.dtype == torch.bfloat16 else FA_DTYPE_F32, lse.data_ptr(),
+                                      bias.data_ptr(), sb, sh, sq,
+                                      seqlens_q.data_ptr() if seqlens_q is not None else 0,
+                                      seqlens_k.data_ptr() if seqlens_k is not None else 0,
+                                      B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
     return o, lse
 
 

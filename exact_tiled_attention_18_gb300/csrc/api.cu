@@ -126,8 +126,15 @@ fa::SchedParams make_sched(int heads, int n, int d, int causal, int grid_cap, lo
 
 fa_status fwd_common(const void* q, const void* k, const void* v, void* o, int o_dtype, float* lse,
                      const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
-                     int causal, fa_stream_t stream) {
+                     int causal, fa_stream_t stream, const void* bias = nullptr, long long bias_sb = 0,
+                     long long bias_sh = 0, long long bias_sq = 0) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (bias) {
+    // strides in elements, whole 16-byte groups (8 bf16); a query stride of 0
+    // broadcasts one row of key biases over the queries, otherwise rows hold Nk keys
+    if (bias_sb < 0 || bias_sh < 0 || bias_sq < 0 || (bias_sq != 0 && bias_sq < Nk)) return FA_ERR_INVALID_ARG;
+    if (!aligned(bias, 2)) return FA_ERR_MISALIGNED;
+  }
   if (o_dtype != FA_DTYPE_F32 && o_dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   fa_status st = check_sizes(B, H, Nq, d, causal);
   if (st != FA_OK) return st;
@@ -160,6 +167,10 @@ fa_status fwd_common(const void* q, const void* k, const void* v, void* o, int o
   a.status = di.status;
   a.wait_limit_ns = wait_limit_ns();
   a.stall_unit = test_stall_unit();
+  a.bias = static_cast<const uint16_t*>(bias);
+  a.bias_sb = bias_sb;
+  a.bias_sh = bias_sh;
+  a.bias_sq = bias_sq;
   return fa::launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -259,6 +270,15 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int o_
                     const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
                     int causal, fa_stream_t stream) {
   return fwd_common(q, k, v, o, o_dtype, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream);
+}
+
+fa_status fa_fwd_bias(const void* q, const void* k, const void* v, void* o, int o_dtype, float* lse,
+                      const void* bias, long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,
+                      const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
+                      int causal, fa_stream_t stream) {
+  if (!bias) return FA_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o, o_dtype, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream, bias,
+                    bias_stride_b, bias_stride_h, bias_stride_q);
 }
 
 size_t fa_fwd_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {

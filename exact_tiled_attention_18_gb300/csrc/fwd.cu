@@ -52,6 +52,7 @@ static_assert(2 * 128 * kFwdSoftmaxRegs + 128 * kFwdOtherRegs <= kFwdThreads * k
               "register split exceeds the launch allocation");
 constexpr float kTau = 8.0f;  // lazy-rescale threshold, log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.4426950408889634f;
 
 enum FwdSite : int {
   SITE_LOAD_Q = 1,
@@ -133,12 +134,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool BIAS>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o, float* __restrict__ lse,
                const int o_bf16, const SeqGeom geom, const float scale_log2, const SchedParams sp,
-               int* status, const unsigned long long limit_ns, const int stall_unit) {
+               int* status, const unsigned long long limit_ns, const int stall_unit,
+               const uint16_t* __restrict__ bias, const long long bias_sb, const long long bias_sh,
+               const long long bias_sq) {
   using L = FwdLayout<D>;
   constexpr int S = L::kSlots;
   extern __shared__ uint8_t smem_raw[];
@@ -206,6 +209,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int row = qtile * kTileRows + r;
       const int unit = head * sp.units_per_head + pair;
       float m_ref = 0.f, l = 0.f;
+      // additive mask: this row's bias (bf16, keys contiguous), none for
+      // padding rows (fully masked anyway)
+      const uint16_t* brow = nullptr;
+      bool bvec = false;  // row start 16-byte aligned: whole tiles in 16-byte loads
+      if constexpr (BIAS) {
+        const int bidx = head / geom.heads_per_batch;
+        if (row < u.lq) {
+          brow = bias + bidx * bias_sb + (head - bidx * geom.heads_per_batch) * bias_sh +
+                 static_cast<long long>(row) * bias_sq;
+          bvec = (reinterpret_cast<uintptr_t>(brow) & 15) == 0;
+        }
+      }
       if (VARLEN && nt == 0) {
         // no key for any row of this tile (or all padding): O = 0, LSE = -inf
         if (row < nq) {
@@ -219,17 +234,67 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         continue;
       }
       for (int j = 0; j < nt; ++j) {
+        // bias of this row's 128 keys of tile j, fetched while S(j) is computed
+        uint4 bq[BIAS ? 16 : 1];
+        if constexpr (BIAS) {
+          const int col0 = j * kTileRows;
+          if (bvec && col0 + kTileRows <= geom.nk) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) bq[i] = __ldg(reinterpret_cast<const uint4*>(brow + col0) + i);
+          } else {
+            // a row that is not 16-byte aligned, the tile past the end of
+            // the bias rows, or a padding row: element loads; keys from Nk on
+            // are masked, their bias is never used
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c0 = col0 + 8 * i + 2 * e;
+                const uint32_t lo = (brow && c0 < geom.nk) ? brow[c0] : 0u;
+                const uint32_t hi = (brow && c0 + 1 < geom.nk) ? brow[c0 + 1] : 0u;
+                w[e] = lo | (hi << 16);
+              }
+              bq[i] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
         ok = warp_wait(BAR(L::S_FULL + t), sn & 1, wc, SITE_SOFTMAX_S, unit);
         if (!ok) break;
         ++sn;
         tc_fence_after();
-        uint32_t sr[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
-        tmem_ld_wait();
         float s[128];
+        if constexpr (BIAS) {
+          // t = s * scale * log2(e) + bias * log2(e): the max and the
+          // exponentials below work on t directly (log2 units); S is read a
+          // chunk at a time so that the bias registers free up as it goes
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t sr[32];
+            tmem_ld32(tS + 32 * c, sr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 b4 = bq[4 * c + i];
+              const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int col = 32 * c + 8 * i + 2 * e;
+                s[col] = fmaf(__uint_as_float(sr[8 * i + 2 * e]), scale_log2,
+                              __uint_as_float(bw[e] << 16) * kLog2e);
+                s[col + 1] = fmaf(__uint_as_float(sr[8 * i + 2 * e + 1]), scale_log2,
+                                  __uint_as_float(bw[e] & 0xFFFF0000u) * kLog2e);
+              }
+            }
+          }
+        } else {
+          uint32_t sr[128];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * c));
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        }
         // keys past the valid length, or (causal) past the row's last key; a
         // padding row masks every key, so that it never takes part in the
         // warp's rescale vote and its values cannot change valid rows' rounding
@@ -253,16 +318,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float t3[5];
 #pragma unroll
         for (int c = 0; c < 5; ++c) t3[c] = fmax3(t2[3 * c], t2[3 * c + 1], t2[3 * c + 2]);
-        const float mt = fmaxf(fmax3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4])) * scale_log2;
+        const float mt = fmaxf(fmax3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4])) * (BIAS ? 1.f : scale_log2);
         if (j == 0) {
-          m_ref = (mt == -CUDART_INF_F) ? 0.f : mt;
+          // without a bias the first key tile holds a key of every row that
+          // has one; with a bias it may hide them all, so the reference stays
+          // -inf until a finite maximum appears
+          m_ref = (mt == -CUDART_INF_F && !BIAS) ? 0.f : mt;
         } else {
           const bool need = mt > m_ref + kTau;
           if (__any_sync(0xffffffffu, need)) {
             // move the reference and rescale l and the accumulator together;
             // PV of the previous tile is complete (its commit preceded S(j)'s)
             const float m_new = fmaxf(m_ref, mt);
-            const float alpha = ex2_approx(m_ref - m_new);
+            const float alpha = (BIAS && m_new == -CUDART_INF_F) ? 1.f : ex2_approx(m_ref - m_new);
             m_ref = m_new;
             l *= alpha;
 #pragma unroll 1
@@ -279,8 +347,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         // P = 2^(s*c - m_ref) in bf16 over the first 64 S columns; two lanes
         // of the scale-subtract and of the running sum per instruction
-        const uint64_t c2 = f2_pack(scale_log2, scale_log2);
-        const uint64_t n2 = f2_pack(-m_ref, -m_ref);
+        const float cexp = BIAS ? 1.f : scale_log2;
+        const float m_use = (BIAS && m_ref == -CUDART_INF_F) ? 0.f : m_ref;  // every t is -inf then
+        const uint64_t c2 = f2_pack(cexp, cexp);
+        const uint64_t n2 = f2_pack(-m_use, -m_use);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -528,10 +598,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool VARLEN>
+template <int D, bool CAUSAL, bool VARLEN, bool BIAS = false>
 cudaError_t launch_fwd_v(const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto kern = fwd_kernel<D, CAUSAL, VARLEN>;
+  auto kern = fwd_kernel<D, CAUSAL, VARLEN, BIAS>;
   cudaFuncAttributes fattr;
   cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
   if (e != cudaSuccess) return e;
@@ -541,12 +611,14 @@ cudaError_t launch_fwd_v(const FwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   kern<<<a.sched.grid, kFwdThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.o_bf16, a.geom,
                                                              a.scale_log2, a.sched, a.status, a.wait_limit_ns,
-                                                             a.stall_unit);
+                                                             a.stall_unit, a.bias, a.bias_sb, a.bias_sh,
+                                                             a.bias_sq);
   return cudaGetLastError();
 }
 
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  if (a.bias) return launch_fwd_v<D, CAUSAL, true, true>(a, stream);
   const bool square = !a.geom.seqlens_q && !a.geom.seqlens_k && a.geom.nq == a.geom.nk && !a.o_bf16;
   return square ? launch_fwd_v<D, CAUSAL, false>(a, stream) : launch_fwd_v<D, CAUSAL, true>(a, stream);
 }

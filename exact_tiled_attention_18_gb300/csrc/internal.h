@@ -32,6 +32,8 @@ struct FwdArgs {
   int* status;                   // device status word (4 ints)
   unsigned long long wait_limit_ns;
   int stall_unit;                // testing: CTA 0 skips one K tile of its n-th unit (-1: never)
+  const uint16_t* bias;          // additive mask, bf16, or null; element (b, h, i, j) at
+  long long bias_sb, bias_sh, bias_sq;  //   b * bias_sb + h * bias_sh + i * bias_sq + j
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);

@@ -135,6 +135,31 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int o_
                     int causal, fa_stream_t stream);
 
 /*
+ * Forward pass with a general additive mask: the "+ mask" of the definition
+ * weights = row_softmax(scores + mask) ("FlashAttention Interview Questions
+ * ...", section "What is FlashAttention exact about?") as a bias added to
+ * the scaled scores, s_ij = scale * q_i.k_j + bias_ij.  It is not scaled; an
+ * entry of -inf hides the key; it combines with the causal rule and with
+ * padding, and a row whose keys are all hidden gets O = 0, LSE = -inf.
+ *   bias  : bf16, element (b, h, i, j) at
+ *           bias + b*bias_stride_b + h*bias_stride_h + i*bias_stride_q + j,
+ *           keys contiguous.  Strides in elements, >= 0; 0 broadcasts over
+ *           that index (bias_stride_q = 0: one row of key biases for every
+ *           query, e.g. a key-padding mask); otherwise bias_stride_q >= Nk.
+ *           2-byte aligned.  Rows that start on a 16-byte boundary (base
+ *           16-byte aligned, strides multiples of 8) are read in 16-byte
+ *           loads, others element by element (slower).  No +inf, no NaN.
+ * Other arguments, results and errors as fa_fwd_ex; a null bias or an
+ * invalid stride returns FA_ERR_INVALID_ARG, a bias at an odd address
+ * FA_ERR_MISALIGNED.  The backward entry points do not take a bias:
+ * gradients of a masked forward are outside this library.
+ */
+fa_status fa_fwd_bias(const void* q, const void* k, const void* v, void* o, int o_dtype, float* lse,
+                      const void* bias, long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,
+                      const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
+                      int causal, fa_stream_t stream);
+
+/*
  * Decode-shaped forward: 1 <= Nq <= FA_DECODE_MAX_Q query rows per head
  * against a long key/value history.  Computes exactly what fa_fwd_varlen
  * computes for the same arguments (same layouts, lengths, bottom-right causal
