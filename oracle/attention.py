@@ -183,10 +183,12 @@ def forward_varlen(q, k, v, scale, causal, seqlens_q, seqlens_k, bias=None):
     return o, lse
 
 
-def backward_head(q, k, v, do, scale, causal, lse=None):
+def backward_head(q, k, v, do, scale, causal, lse=None, bias=None):
     """Gradient of sum(O * dO) with respect to q, k, v for one head.
 
-    Chain rule of the definition, with P_ij = exp(s_ij - LSE_i):
+    Chain rule of the definition, with P_ij = exp(s_ij - LSE_i) and s_ij the
+    masked score (scale * q_i.k_j plus the additive ``bias`` [Nq, Nk] when
+    given; the bias is a constant of the differentiation):
       dV_j  = sum_i P_ij dO_i
       dP_ij = <dO_i, v_j>
       D_i   = sum_j P_ij dP_ij
@@ -195,9 +197,9 @@ def backward_head(q, k, v, do, scale, causal, lse=None):
       dK_j  = scale * sum_i dS_ij q_i
     Returns (dQ, dK, dV, D).
     """
-    s, ok = _masked_scores(q, k, scale, causal)
+    s, ok = _masked_scores(q, k, scale, causal, bias)
     if lse is None:
-        _, lse = forward_head(q, k, v, scale, causal)
+        _, lse = forward_head(q, k, v, scale, causal, bias)
     has_key = np.isfinite(lse)
     p = np.where(ok & has_key[:, None], np.exp(s - np.where(has_key, lse, 0.0)[:, None]), 0.0)
     dv = p.T @ do
@@ -209,8 +211,9 @@ def backward_head(q, k, v, do, scale, causal, lse=None):
     return dq, dk, dv, dd
 
 
-def backward(q, k, v, do, scale, causal):
-    """Gradients over [B, H, N, d] arrays; returns (dQ, dK, dV, D)."""
+def backward(q, k, v, do, scale, causal, bias=None):
+    """Gradients over [B, H, N, d] arrays (``bias``: None or [B, H, Nq, Nk]
+    additive mask); returns (dQ, dK, dV, D)."""
     b, h, n, d = q.shape
     dq = np.empty_like(q, dtype=np.float64)
     dk = np.empty_like(k, dtype=np.float64)
@@ -219,13 +222,14 @@ def backward(q, k, v, do, scale, causal):
     for bi in range(b):
         for hi in range(h):
             dq[bi, hi], dk[bi, hi], dv[bi, hi], dd[bi, hi] = backward_head(
-                q[bi, hi], k[bi, hi], v[bi, hi], do[bi, hi], scale, causal)
+                q[bi, hi], k[bi, hi], v[bi, hi], do[bi, hi], scale, causal,
+                bias=None if bias is None else bias[bi, hi])
     return dq, dk, dv, dd
 
 
-def backward_varlen(q, k, v, do, scale, causal, seqlens_q, seqlens_k):
-    """Gradients of a padded batch (see forward_varlen); padding rows of dQ,
-    dK, dV and D are 0.  Returns (dQ, dK, dV, D)."""
+def backward_varlen(q, k, v, do, scale, causal, seqlens_q, seqlens_k, bias=None):
+    """Gradients of a padded batch (see forward_varlen; ``bias`` as there);
+    padding rows of dQ, dK, dV and D are 0.  Returns (dQ, dK, dV, D)."""
     b, h, nq, _ = q.shape
     dq = np.zeros(q.shape, dtype=np.float64)
     dk = np.zeros(k.shape, dtype=np.float64)
@@ -235,7 +239,8 @@ def backward_varlen(q, k, v, do, scale, causal, seqlens_q, seqlens_k):
         lq, lk = int(seqlens_q[bi]), int(seqlens_k[bi])
         for hi in range(h):
             gq, gk, gv, gd = backward_head(q[bi, hi, :lq], k[bi, hi, :lk], v[bi, hi, :lk], do[bi, hi, :lq],
-                                           scale, causal)
+                                           scale, causal,
+                                           bias=None if bias is None else bias[bi, hi, :lq, :lk])
             dq[bi, hi, :lq], dk[bi, hi, :lk], dv[bi, hi, :lk], dd[bi, hi, :lq] = gq, gk, gv, gd
     return dq, dk, dv, dd
 

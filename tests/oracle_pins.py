@@ -193,18 +193,21 @@ def _to_mp(a):
 
 
 @functools.lru_cache(maxsize=None)
-def _brute(nq, nk, d, causal, seed):
+def _brute(nq, nk, d, causal, seed, with_bias=False):
     """50-digit forward values and central-difference gradients of
-    sum(O * dO) for one random head with nq queries and nk keys."""
+    sum(O * dO) for one random head with nq queries and nk keys (with a
+    random finite additive mask when ``with_bias``)."""
     mpmath.mp.dps = 50
     q, do = (_bf16_values((nq, d), seed + t) for t in (0, 3))
     k, v = (_bf16_values((nk, d), seed + t) for t in (1, 2))
+    bias = np.random.default_rng(seed + 9).standard_normal((nq, nk)) * 1.5 if with_bias else None
+    B = _to_mp(bias) if with_bias else None
     scale = mpmath.mpf(1) / mpmath.sqrt(d)
     Q, K, V, DO = _to_mp(q), _to_mp(k), _to_mp(v), _to_mp(do)
-    o, lse = _mp_forward(Q, K, V, scale, causal)
+    o, lse = _mp_forward(Q, K, V, scale, causal, B)
 
     def f(Q_, K_, V_):
-        oo, _ = _mp_forward(Q_, K_, V_, scale, causal)
+        oo, _ = _mp_forward(Q_, K_, V_, scale, causal, B)
         return mpmath.fsum(oo[i][c] * DO[i][c] for i in range(nq) for c in range(d))
 
     h = mpmath.mpf("1e-18")
@@ -223,17 +226,18 @@ def _brute(nq, nk, d, causal, seed):
         grads.append(g)
     o_np = np.array([[float(x) for x in row] for row in o])
     lse_np = np.array([float(x) for x in lse])
-    return (q, k, v, do, float(scale), o_np, lse_np) + tuple(grads)
+    return (q, k, v, do, float(scale), o_np, lse_np, bias) + tuple(grads)
 
 
-def _check_brute(ora, nq, nk, d, causal, seed):
-    q, k, v, do, scale, o_ref, lse_ref, dq_ref, dk_ref, dv_ref = _brute(nq, nk, d, causal, seed)
-    o, lse = ora.forward(_head(q), _head(k), _head(v), scale, causal)
+def _check_brute(ora, nq, nk, d, causal, seed, with_bias=False):
+    q, k, v, do, scale, o_ref, lse_ref, bias, dq_ref, dk_ref, dv_ref = _brute(nq, nk, d, causal, seed, with_bias)
+    b4 = None if bias is None else bias[None, None]
+    o, lse = ora.forward(_head(q), _head(k), _head(v), scale, causal, b4)
     assert np.max(np.abs(o[0, 0] - o_ref)) < 1e-13, np.max(np.abs(o[0, 0] - o_ref))
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(lse[0, 0]), fin)
     assert np.max(np.abs(lse[0, 0][fin] - lse_ref[fin]), initial=0.0) < 1e-13
-    dq, dk, dv, _ = ora.backward(_head(q), _head(k), _head(v), _head(do), scale, causal)
+    dq, dk, dv, _ = ora.backward(_head(q), _head(k), _head(v), _head(do), scale, causal, b4)
     for got, ref in ((dq, dq_ref), (dk, dk_ref), (dv, dv_ref)):
         assert np.max(np.abs(got[0, 0] - ref)) < 1e-12, np.max(np.abs(got[0, 0] - ref))
 
@@ -397,6 +401,48 @@ def check_brute_force_bias(ora):
     assert np.max(np.abs(lse[0, 0] - lse_ref)) < 1e-13
 
 
+def check_brute_force_bias_gradients(ora):
+    """Gradients under a random additive mask against 50-digit central
+    differences of the masked definition (causal and not, unequal lengths)."""
+    _check_brute(ora, 4, 6, 4, True, 801, with_bias=True)
+    _check_brute(ora, 5, 5, 4, False, 901, with_bias=True)
+
+
+def check_bias_backward_masks_like_causal(ora):
+    """Gradients under a 0 / -inf mask shaped like the causal rule equal the
+    causal gradients (padded batch, bottom-right alignment)."""
+    rng = np.random.default_rng(67)
+    q, do = rng.standard_normal((2, 1, 1, 6, 4))
+    k, v = rng.standard_normal((2, 1, 1, 9, 4))
+    i = np.arange(6)[:, None]
+    j = np.arange(9)[None, :]
+    bias = np.where(j <= i + 3, 0.0, -np.inf)[None, None]
+    a = ora.backward(q, k, v, do, 0.5, True)
+    b = ora.backward(q, k, v, do, 0.5, False, bias)
+    for x, y in zip(a, b):
+        assert np.max(np.abs(x - y)) < 1e-13
+    lq, lk = [5], [7]
+    bias_v = np.where(j <= i + 2, 0.0, -np.inf)[None, None]
+    a = ora.backward_varlen(q, k, v, do, 0.5, True, lq, lk)
+    b = ora.backward_varlen(q, k, v, do, 0.5, False, lq, lk, bias_v)
+    for x, y in zip(a, b):
+        assert np.max(np.abs(x - y)) < 1e-13
+
+
+def check_bias_backward_hidden_row(ora):
+    """A row the mask hides entirely has zero gradient and adds nothing to
+    dK and dV."""
+    q, k, v, do = _random_case(1, 1, 5, 4, 68)
+    bias = np.random.default_rng(69).standard_normal((1, 1, 5, 5))
+    bias[0, 0, 3, :] = -np.inf
+    dq, dk, dv, dd = ora.backward(q, k, v, do, 0.5, False, bias)
+    assert np.all(dq[0, 0, 3] == 0) and dd[0, 0, 3] == 0
+    keep = [0, 1, 2, 4]
+    dq2, dk2, dv2, _ = ora.backward(q[:, :, keep], k, v, do[:, :, keep], 0.5, False, bias[:, :, keep])
+    assert np.max(np.abs(dk - dk2)) < 1e-14 and np.max(np.abs(dv - dv2)) < 1e-14
+    assert np.max(np.abs(dq[0, 0, keep] - dq2[0, 0])) < 1e-14
+
+
 def check_forward_rows_with_bias(ora):
     """The row sampler sees the same bias as the full forward."""
     q, k, v, _ = _random_case(2, 2, 13, 8, 65)
@@ -433,6 +479,9 @@ ALL_CHECKS = [
     check_bias_fully_hidden_row,
     check_brute_force_bias,
     check_forward_rows_with_bias,
+    check_brute_force_bias_gradients,
+    check_bias_backward_masks_like_causal,
+    check_bias_backward_hidden_row,
 ]
 
 

@@ -33,6 +33,11 @@ MUTATIONS = {
     "bias_transposed": ("        s = s + bias\n        ok", "        s = s + bias.T\n        ok"),
     "bias_sign_flipped": ("        s = s + bias\n        ok", "        s = s - bias\n        ok"),
     "rows_bias_ignored": ("            s = s + bias[bi, hi, i, :count]", "            s = s + 0.0"),
+    "backward_bias_ignored": ("    s, ok = _masked_scores(q, k, scale, causal, bias)\n    if lse is None:",
+                              "    s, ok = _masked_scores(q, k, scale, causal)\n    if lse is None:"),
+    "backward_lse_without_bias": ("_, lse = forward_head(q, k, v, scale, causal, bias)",
+                                  "_, lse = forward_head(q, k, v, scale, causal)"),
+    "varlen_backward_bias_dropped": ("bias=None if bias is None else bias[bi, hi, :lq, :lk])", "bias=None)"),
     "varlen_keys_sliced_by_query_length": ("v[bi, hi, :lk],\n                                                            scale", "v[bi, hi, :lq],\n                                                            scale"),
 }
 
