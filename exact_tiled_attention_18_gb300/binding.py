@@ -58,6 +58,9 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_bias.restype = st
         L.fa_bwd_ex.argtypes = [vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_bwd_ex.restype = st
+        L.fa_bwd_bias.argtypes = [vp, vp, vp, vp, i, vp, vp, vp, ll, ll, ll, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
+                                  i, vp]
+        L.fa_bwd_bias.restype = st
         L.fa_fwd_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_fwd_decode.restype = st
         L.fa_fwd_decode_workspace_bytes.argtypes = [i, i, i, i, i]
@@ -122,6 +125,14 @@ def fa_bwd_ex(q: int, k: int, v: int, o: int, o_dtype: int, lse: int, do: int, d
               causal: int, stream: int) -> int:
     return lib().fa_bwd_ex(q, k, v, o, o_dtype, lse, do, dq, dk, dv, workspace, seqlens_q, seqlens_k, B, H, Nq, Nk,
                            d, scale, causal, stream)
+
+
+def fa_bwd_bias(q: int, k: int, v: int, o: int, o_dtype: int, lse: int, do: int, bias: int, bias_stride_b: int,
+                bias_stride_h: int, bias_stride_q: int, dq: int, dk: int, dv: int, workspace: int, seqlens_q: int,
+                seqlens_k: int, B: int, H: int, Nq: int, Nk: int, d: int, scale: float, causal: int,
+                stream: int) -> int:
+    return lib().fa_bwd_bias(q, k, v, o, o_dtype, lse, do, bias, bias_stride_b, bias_stride_h, bias_stride_q, dq, dk,
+                             dv, workspace, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream)
 
 
 def fa_fwd_decode(q: int, k: int, v: int, o: int, lse: int, seqlens_q: int, seqlens_k: int, workspace: int, B: int,
@@ -264,6 +275,18 @@ def forward_varlen(q, k, v, seqlens_q=None, seqlens_k=None, causal: bool = False
     return o, lse
 
 
+def _bias_strides(bias, B, H, Nq, Nk):
+    """Element strides (b, h, query) of a bf16 CUDA mask broadcastable to
+    [B, H, Nq, Nk] with contiguous keys."""
+    import torch
+    if not bias.is_cuda or bias.dtype != torch.bfloat16:
+        raise ValueError("bias must be a bf16 CUDA tensor")
+    bias = bias.expand(B, H, Nq, Nk)
+    if bias.stride(3) != 1:
+        raise ValueError("the bias's key dimension must be contiguous")
+    return bias.stride(0), bias.stride(1), bias.stride(2)
+
+
 def forward_bias(q, k, v, bias, seqlens_q=None, seqlens_k=None, causal: bool = False, scale: float | None = None,
                  o_dtype=None, out=None):
     """O, LSE through fa_fwd_bias: softmax(scale * q k^T + bias) v.  ``bias``
@@ -278,11 +301,7 @@ def forward_bias(q, k, v, bias, seqlens_q=None, seqlens_k=None, causal: bool = F
     Nk = k.shape[2]
     if k.shape != (B, H, Nk, d) or v.shape != k.shape:
         raise ValueError("k and v must be [B, H, Nk, d] with the batch, heads and d of q")
-    if not bias.is_cuda or bias.dtype != torch.bfloat16:
-        raise ValueError("bias must be a bf16 CUDA tensor")
-    bias = bias.expand(B, H, Nq, Nk)
-    if bias.stride(3) != 1:
-        raise ValueError("the bias's key dimension must be contiguous")
+    sb, sh, sq = _bias_strides(bias, B, H, Nq, Nk)
     for t in (seqlens_q, seqlens_k):
         if t is not None and (not t.is_cuda or t.dtype != torch.int32 or t.numel() != B or not t.is_contiguous()):
             raise ValueError("seqlens must be contiguous int32 CUDA tensors of B entries")
@@ -295,7 +314,6 @@ def forward_bias(q, k, v, bias, seqlens_q=None, seqlens_k=None, causal: bool = F
         o, lse = out
     if o.dtype not in (torch.float32, torch.bfloat16):
         raise ValueError("O must be float32 or bfloat16")
-    sb, sh, sq, _ = bias.stride()
     _check("fa_fwd_bias", fa_fwd_bias(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                       FA_DTYPE_BF16 if o.dtype == torch.bfloat16 else FA_DTYPE_F32, lse.data_ptr(),
                                       bias.data_ptr(), sb, sh, sq,
@@ -356,8 +374,20 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
 
 def backward_varlen(q, k, v, o, lse, do, seqlens_q=None, seqlens_k=None, causal: bool = False,
                     scale: float | None = None, workspace=None, out=None):
-    """dQ, dK, dV through fa_bwd_varlen: q, do, o [B,H,Nq,d], lse [B,H,Nq],
-    k and v [B,H,Nk,d]; seqlens as forward_varlen (fp32 outputs)."""
+    """dQ, dK, dV through fa_bwd_ex: q, do, o [B,H,Nq,d] (o fp32 or bf16),
+    lse [B,H,Nq], k and v [B,H,Nk,d]; seqlens as forward_varlen (fp32
+    outputs)."""
+    return _backward(q, k, v, o, lse, do, None, seqlens_q, seqlens_k, causal, scale, workspace, out)
+
+
+def backward_bias(q, k, v, o, lse, do, bias, seqlens_q=None, seqlens_k=None, causal: bool = False,
+                  scale: float | None = None, workspace=None, out=None):
+    """dQ, dK, dV of forward_bias through fa_bwd_bias; ``bias`` exactly as
+    given to forward_bias, other arguments as backward_varlen."""
+    return _backward(q, k, v, o, lse, do, bias, seqlens_q, seqlens_k, causal, scale, workspace, out)
+
+
+def _backward(q, k, v, o, lse, do, bias, seqlens_q, seqlens_k, causal, scale, workspace, out):
     import torch
     for t in (q, k, v, do):
         if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
@@ -380,12 +410,19 @@ def backward_varlen(q, k, v, o, lse, do, seqlens_q=None, seqlens_k=None, causal:
     if o.dtype not in (torch.float32, torch.bfloat16):
         raise ValueError("O must be float32 or bfloat16")
     o_dtype = FA_DTYPE_BF16 if o.dtype == torch.bfloat16 else FA_DTYPE_F32
-    _check("fa_bwd_ex",
-           fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o_dtype, lse.data_ptr(), do.data_ptr(),
-                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws,
-                     seqlens_q.data_ptr() if seqlens_q is not None else 0,
-                     seqlens_k.data_ptr() if seqlens_k is not None else 0,
-                     B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    lq = seqlens_q.data_ptr() if seqlens_q is not None else 0
+    lk = seqlens_k.data_ptr() if seqlens_k is not None else 0
+    if bias is None:
+        _check("fa_bwd_ex",
+               fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o_dtype, lse.data_ptr(),
+                         do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws, lq, lk,
+                         B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    else:
+        sb, sh, sq = _bias_strides(bias, B, H, Nq, Nk)
+        _check("fa_bwd_bias",
+               fa_bwd_bias(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), o_dtype, lse.data_ptr(),
+                           do.data_ptr(), bias.data_ptr(), sb, sh, sq, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                           ws, lq, lk, B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
     return dq, dk, dv
 
 

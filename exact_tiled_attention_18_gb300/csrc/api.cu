@@ -124,16 +124,23 @@ fa::SchedParams make_sched(int heads, int n, int d, int causal, int grid_cap, lo
   return sp;
 }
 
+// Strides in elements; a query stride of 0 broadcasts one row of key
+// biases over the queries, otherwise rows hold Nk keys.
+fa_status check_bias(const void* bias, long long sb, long long sh, long long sq, int Nk) {
+  if (!bias) return FA_ERR_INVALID_ARG;
+  if (sb < 0 || sh < 0 || sq < 0 || (sq != 0 && sq < Nk)) return FA_ERR_INVALID_ARG;
+  if (!aligned(bias, 2)) return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
 fa_status fwd_common(const void* q, const void* k, const void* v, void* o, int o_dtype, float* lse,
                      const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
                      int causal, fa_stream_t stream, const void* bias = nullptr, long long bias_sb = 0,
                      long long bias_sh = 0, long long bias_sq = 0) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (bias) {
-    // strides in elements, whole 16-byte groups (8 bf16); a query stride of 0
-    // broadcasts one row of key biases over the queries, otherwise rows hold Nk keys
-    if (bias_sb < 0 || bias_sh < 0 || bias_sq < 0 || (bias_sq != 0 && bias_sq < Nk)) return FA_ERR_INVALID_ARG;
-    if (!aligned(bias, 2)) return FA_ERR_MISALIGNED;
+    const fa_status bs = check_bias(bias, bias_sb, bias_sh, bias_sq, Nk);
+    if (bs != FA_OK) return bs;
   }
   if (o_dtype != FA_DTYPE_F32 && o_dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   fa_status st = check_sizes(B, H, Nq, d, causal);
@@ -251,6 +258,25 @@ void decode_splits(int heads, int Nk, int sms, int& splits, int& chunk) {
   splits = (Nk + chunk - 1) / chunk;
 }
 
+// Both backward kernels on prepared arguments; without a workspace the row
+// term lives in a stream-ordered allocation freed behind the kernels.
+fa_status bwd_launch(fa::BwdArgs& a, float* workspace, int B, int H, int Nq, fa_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* delta = workspace;
+  if (!delta) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&delta), fa_bwd_workspace_bytes(B, H, Nq), s) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+  }
+  a.delta = delta;
+  cudaError_t e = fa::launch_bwd(a, s);
+  if (!workspace) {
+    cudaError_t e2 = cudaFreeAsync(delta, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+
 }  // namespace
 
 extern "C" {
@@ -276,7 +302,7 @@ fa_status fa_fwd_bias(const void* q, const void* k, const void* v, void* o, int 
                       const void* bias, long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,
                       const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
                       int causal, fa_stream_t stream) {
-  if (!bias) return FA_ERR_INVALID_ARG;
+  if (!bias) return FA_ERR_INVALID_ARG;  // fwd_common treats null as no mask
   return fwd_common(q, k, v, o, o_dtype, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream, bias,
                     bias_stride_b, bias_stride_h, bias_stride_q);
 }
@@ -352,19 +378,22 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
   fa_status st = bwd_prepare(a, q, k, v, o, o_dtype, lse, dO, dq, dk, dv, workspace, seqlens_q, seqlens_k, B, H, Nq,
                              Nk, d, scale, causal);
   if (st != FA_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float* delta = workspace;
-  if (!delta) {
-    if (cudaMallocAsync(reinterpret_cast<void**>(&delta), fa_bwd_workspace_bytes(B, H, Nq), s) != cudaSuccess)
-      return FA_ERR_LAUNCH;
-  }
-  a.delta = delta;
-  cudaError_t e = fa::launch_bwd(a, s);
-  if (!workspace) {
-    cudaError_t e2 = cudaFreeAsync(delta, s);
-    if (e == cudaSuccess) e = e2;
-  }
-  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  return bwd_launch(a, workspace, B, H, Nq, stream);
+}
+
+fa_status fa_bwd_bias(const void* q, const void* k, const void* v, const void* o, int o_dtype, const float* lse,
+                      const void* dO, const void* bias, long long bias_stride_b, long long bias_stride_h,
+                      long long bias_stride_q, float* dq, float* dk, float* dv, float* workspace,
+                      const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
+                      int causal, fa_stream_t stream) {
+  fa_status st = check_bias(bias, bias_stride_b, bias_stride_h, bias_stride_q, Nk);
+  if (st != FA_OK) return st;
+  fa::BwdArgs a;
+  st = bwd_prepare(a, q, k, v, o, o_dtype, lse, dO, dq, dk, dv, workspace, seqlens_q, seqlens_k, B, H, Nq, Nk, d,
+                   scale, causal);
+  if (st != FA_OK) return st;
+  a.bias = fa::BiasRef{static_cast<const uint16_t*>(bias), bias_stride_b, bias_stride_h, bias_stride_q};
+  return bwd_launch(a, workspace, B, H, Nq, stream);
 }
 
 fa_status fa_bwd_varlen(const void* q, const void* k, const void* v, const float* o, const float* lse,

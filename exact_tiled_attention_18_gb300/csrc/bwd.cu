@@ -94,6 +94,58 @@ __device__ __forceinline__ uint64_t f2_from(uint32_t a, uint32_t b) {
   return f2_pack(__uint_as_float(a), __uint_as_float(b));
 }
 
+// a pair of bf16 values (low half first) widened to an fp32 pair
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t u) {
+  return f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
+// Additive mask of one key for 64 consecutive queries q0.. (a column of the
+// mask, stride sq elements), as bf16 pairs: queries q0..q0+31 in b0,
+// q0+32..q0+63 in b1; 0 past query nq or without a column.  Across a warp
+// (32 consecutive keys) each load is one contiguous 64-byte segment.
+__device__ __forceinline__ void load_bias_column(const uint16_t* bcol, long long sq, int q0, int nq,
+                                                 uint32_t (&b0)[16], uint32_t (&b1)[16]) {
+  uint32_t h[64];
+  if (bcol && q0 + 64 <= nq) {
+    const uint16_t* p = bcol + q0 * sq;
+#pragma unroll
+    for (int c = 0; c < 64; ++c) h[c] = __ldg(p + c * sq);
+  } else {
+#pragma unroll
+    for (int c = 0; c < 64; ++c) h[c] = (bcol && q0 + c < nq) ? __ldg(bcol + (q0 + c) * sq) : 0u;
+  }
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    b0[e] = h[2 * e] | (h[2 * e + 1] << 16);
+    b1[e] = h[32 + 2 * e] | (h[33 + 2 * e] << 16);
+  }
+}
+
+// Additive mask of one query for 64 consecutive keys k0.. (part of a row),
+// as bf16 pairs: keys k0..k0+31 in b0, k0+32..k0+63 in b1; 0 past key nk or
+// without a row.  vec: the row starts on a 16-byte boundary (k0 is a
+// multiple of 64, so then every load below is aligned).
+__device__ __forceinline__ void load_bias_row(const uint16_t* brow, bool vec, int k0, int nk, uint32_t (&b0)[16],
+                                              uint32_t (&b1)[16]) {
+  if (vec && k0 + 64 <= nk) {
+    const uint4* p = reinterpret_cast<const uint4*>(brow + k0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 x = __ldg(p + i), y = __ldg(p + 4 + i);
+      b0[4 * i] = x.x, b0[4 * i + 1] = x.y, b0[4 * i + 2] = x.z, b0[4 * i + 3] = x.w;
+      b1[4 * i] = y.x, b1[4 * i + 1] = y.y, b1[4 * i + 2] = y.z, b1[4 * i + 3] = y.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int c = k0 + 2 * e;
+      const uint32_t lo = (brow && c < nk) ? __ldg(brow + c) : 0u;
+      const uint32_t hi = (brow && c + 1 < nk) ? __ldg(brow + c + 1) : 0u;
+      (e < 16 ? b0[e] : b1[e - 16]) = lo | (hi << 16);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ dK / dV
 
 template <int D>
@@ -136,13 +188,14 @@ constexpr int kKvOtherRegs = 136;
 static_assert(2 * 128 * kKvEwRegs + 128 * kKvOtherRegs <= kKvThreads * kKvLaunchRegs,
               "register split exceeds the launch allocation");
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BIAS>
 __global__ void __launch_bounds__(kKvThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const float* __restrict__ lse, const float* __restrict__ delta, float* __restrict__ dk,
                 float* __restrict__ dv, const SeqGeom geom, const float scale, const float scale_log2,
-                const SchedParams sp, int* status, const unsigned long long limit_ns, const int stall_unit) {
+                const SchedParams sp, int* status, const unsigned long long limit_ns, const int stall_unit,
+                const BiasRef bias) {
   using L = KvLayout<D>;
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -205,7 +258,19 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       int i0, i1;
       key_tile_queries(hl, j, CAUSAL, i0, i1);
       const int unit = head * sp.units_per_head + j;
+      // additive mask: this key's column, one element per query at stride sq
+      const uint16_t* bcol = nullptr;
+      if constexpr (BIAS) {
+        const int bidx = head / geom.heads_per_batch;
+        const int key = j * kTileRows + r;
+        if (key < geom.nk)
+          bcol = bias.p + bidx * bias.sb + (head - bidx * geom.heads_per_batch) * bias.sh + key;
+      }
       for (int i = i0; i < i1; ++i) {
+        // the mask of this key for the warpgroup's 64 queries, bf16 pairs
+        // (fetched before the waits; 0 past the last query row)
+        uint32_t bb0[BIAS ? 16 : 1], bb1[BIAS ? 16 : 1];
+        if constexpr (BIAS) load_bias_column(bcol, bias.sq, i * kTileRows + 64 * w, geom.nq, bb0, bb1);
         const uint32_t ls = ldn % S;
         ok = warp_wait(BAR(L::LD_FULL + ls), (ldn / S) & 1, wc, SITE_KV_EW_LD, unit);
         if (!ok) break;
@@ -224,14 +289,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         // Phase 1: P^T for 32 query columns starting at col0, kept in sr as fp32
         // bits and packed to bf16 in pk.  MASKED: a tile crossing the causal
         // boundary, where a key may come after the query.
-        auto pchunk = [&](auto masked, uint32_t (&sr)[32], int col0, uint32_t (&pk)[16]) {
+        auto pchunk = [&](auto masked, uint32_t (&sr)[32], int col0, uint32_t (&pk)[16],
+                          const uint32_t (&bh)[BIAS ? 16 : 1]) {
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
             // l2s holds -LSE*log2(e) (-inf for padding and key-less queries)
             const float4 l4 = *reinterpret_cast<const float4*>(l2s + col0 + c);
+            uint64_t t01 = f2_pack(l4.x, l4.y), t23 = f2_pack(l4.z, l4.w);
+            if constexpr (BIAS) {
+              // + bias * log2(e); a hidden key (-inf) gives p = 0
+              t01 = ffma2(bf16x2_to_f2(bh[c / 2]), f2_pack(kLog2e, kLog2e), t01);
+              t23 = ffma2(bf16x2_to_f2(bh[c / 2 + 1]), f2_pack(kLog2e, kLog2e), t23);
+            }
             float p[4];
-            f2_unpack(ffma2(f2_from(sr[c], sr[c + 1]), c2, f2_pack(l4.x, l4.y)), p[0], p[1]);
-            f2_unpack(ffma2(f2_from(sr[c + 2], sr[c + 3]), c2, f2_pack(l4.z, l4.w)), p[2], p[3]);
+            f2_unpack(ffma2(f2_from(sr[c], sr[c + 1]), c2, t01), p[0], p[1]);
+            f2_unpack(ffma2(f2_from(sr[c + 2], sr[c + 3]), c2, t23), p[2], p[3]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               p[e] = ex2_approx(p[e]);
@@ -270,11 +342,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           tmem_ld32(tS, s0);
           tmem_ld32(tS + 32, s1);
           tmem_ld_wait();
-          if (need_mask) pchunk(std::true_type{}, s0, 64 * w, pk);
-          else pchunk(std::false_type{}, s0, 64 * w, pk);
+          if (need_mask) pchunk(std::true_type{}, s0, 64 * w, pk, bb0);
+          else pchunk(std::false_type{}, s0, 64 * w, pk, bb0);
           tmem_st16(tS, pk);
-          if (need_mask) pchunk(std::true_type{}, s1, 64 * w + 32, pk);
-          else pchunk(std::false_type{}, s1, 64 * w + 32, pk);
+          if (need_mask) pchunk(std::true_type{}, s1, 64 * w + 32, pk, bb1);
+          else pchunk(std::false_type{}, s1, 64 * w + 32, pk, bb1);
           tmem_st16(tS + 16, pk);
           // publish P before taking dP, so that the GEMM reading P (and the
           // next tile's S behind it) queue up while dP is still running
@@ -596,14 +668,14 @@ struct QLayout {
 // register split as dK/dV.
 constexpr int kQThreads = 384;
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BIAS>
 __global__ void __launch_bounds__(kQThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const float* __restrict__ lse, const void* __restrict__ o, const uint16_t* __restrict__ dout,
               const int o_bf16, float* __restrict__ delta, float* __restrict__ dq, const SeqGeom geom,
               const float scale, const float scale_log2, const SchedParams sp, int* status,
-              const unsigned long long limit_ns, const int stall_unit) {
+              const unsigned long long limit_ns, const int stall_unit, const BiasRef bias) {
   using L = QLayout<D>;
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -703,7 +775,20 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const uint64_t nl2x2 = f2_pack(nl2, nl2);
       const uint64_t dd2 = f2_pack(dd, dd);
       float dsum = 0.f;  // this warpgroup's share of delta_i
+      // additive mask: this row's keys (none for padding rows)
+      const uint16_t* brow = nullptr;
+      bool bvec = false;
+      if constexpr (BIAS) {
+        const int bidx = head / geom.heads_per_batch;
+        if (row < hl.lq) {
+          brow = bias.p + bidx * bias.sb + (head - bidx * geom.heads_per_batch) * bias.sh + row * bias.sq;
+          bvec = (reinterpret_cast<uintptr_t>(brow) & 15) == 0;
+        }
+      }
       for (int jt = 0; jt < nk; ++jt) {
+        // the mask of the warpgroup's 64 keys, fetched before the wait
+        uint32_t bb0[BIAS ? 16 : 1], bb1[BIAS ? 16 : 1];
+        if constexpr (BIAS) load_bias_row(brow, bvec, jt * kTileRows + 64 * w, geom.nk, bb0, bb1);
         // P needs only S: dP may still be in the tensor pipe
         const uint32_t sdp_parity = sn & 1;
         ok = warp_wait(BAR(L::S_FULL), sdp_parity, wc, SITE_Q_EW_S, unit);
@@ -719,11 +804,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
         // bits and packed to bf16 in pk.  MASKED: a tile crossing the causal
         // boundary or holding the last valid key, where some key columns are
         // not eligible.
-        auto pchunk = [&](auto masked, uint32_t (&sr)[32], int col0, uint32_t (&pk)[16]) {
+        auto pchunk = [&](auto masked, uint32_t (&sr)[32], int col0, uint32_t (&pk)[16],
+                          const uint32_t (&bh)[BIAS ? 16 : 1]) {
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             float p0, p1;
-            f2_unpack(ffma2(f2_from(sr[c], sr[c + 1]), c2, nl2x2), p0, p1);
+            uint64_t t = nl2x2;
+            // + bias * log2(e); a hidden key (-inf) gives p = 0
+            if constexpr (BIAS) t = ffma2(bf16x2_to_f2(bh[c / 2]), f2_pack(kLog2e, kLog2e), t);
+            f2_unpack(ffma2(f2_from(sr[c], sr[c + 1]), c2, t), p0, p1);
             p0 = ex2_approx(p0);
             p1 = ex2_approx(p1);
             if (decltype(masked)::value) {
@@ -762,11 +851,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
           tmem_ld32(tS, s0);
           tmem_ld32(tS + 32, s1);
           tmem_ld_wait();
-          if (need_mask) pchunk(std::true_type{}, s0, 64 * w, pk);
-          else pchunk(std::false_type{}, s0, 64 * w, pk);
+          if (need_mask) pchunk(std::true_type{}, s0, 64 * w, pk, bb0);
+          else pchunk(std::false_type{}, s0, 64 * w, pk, bb0);
           tmem_st16(tS, pk);
-          if (need_mask) pchunk(std::true_type{}, s1, 64 * w + 32, pk);
-          else pchunk(std::false_type{}, s1, 64 * w + 32, pk);
+          if (need_mask) pchunk(std::true_type{}, s1, 64 * w + 32, pk, bb1);
+          else pchunk(std::false_type{}, s1, 64 * w + 32, pk, bb1);
           tmem_st16(tS + 16, pk);
           // publish P before taking dP, so that the GEMM reading P (and the
           // next tile's S behind it) queue up while dP is still running
@@ -1075,13 +1164,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool BIAS>
 cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
   cudaError_t e = cudaSuccess;
   if (stage == 0) {
     // dQ first: it forms D' = rowsum(dO o O) and turns it into the exact row term
     using L = QLayout<D>;
-    auto kern = dq_kernel<D, CAUSAL>;
+    auto kern = dq_kernel<D, CAUSAL, BIAS>;
     cudaFuncAttributes fattr;
     e = cudaFuncGetAttributes(&fattr, kern);
     if (e != cudaSuccess) return e;
@@ -1090,10 +1179,11 @@ cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     kern<<<a.grid_q, kQThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.o, a.dout,
                                                          a.o_bf16, a.delta, a.dq, a.geom, a.scale, a.scale_log2,
-                                                         a.sched_q, a.status, a.wait_limit_ns, a.stall_unit);
+                                                         a.sched_q, a.status, a.wait_limit_ns, a.stall_unit,
+                                                         a.bias);
   } else {
     using L = KvLayout<D>;
-    auto kern = dkdv_kernel<D, CAUSAL>;
+    auto kern = dkdv_kernel<D, CAUSAL, BIAS>;
     cudaFuncAttributes fattr;
     e = cudaFuncGetAttributes(&fattr, kern);
     if (e != cudaSuccess) return e;
@@ -1103,31 +1193,31 @@ cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     kern<<<a.grid_kv, kKvThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dk,
                                                            a.dv, a.geom, a.scale, a.scale_log2, a.sched_kv, a.status,
-                                                           a.wait_limit_ns, a.stall_unit);
+                                                           a.wait_limit_ns, a.stall_unit, a.bias);
   }
   return cudaGetLastError();
 }
 
 template <int D, bool CAUSAL>
-cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
-  for (int stage = 0; stage < 2; ++stage) {
-    const cudaError_t e = launch_stage_t<D, CAUSAL>(a, stage, stream);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+cudaError_t launch_stage_c(const BwdArgs& a, int stage, cudaStream_t stream) {
+  return a.bias.p ? launch_stage_t<D, CAUSAL, true>(a, stage, stream)
+                  : launch_stage_t<D, CAUSAL, false>(a, stage, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
-  if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
-  return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
-}
-
 cudaError_t launch_bwd_stage(const BwdArgs& a, int stage, cudaStream_t stream) {
   if (a.d == 64)
-    return a.causal ? launch_stage_t<64, true>(a, stage, stream) : launch_stage_t<64, false>(a, stage, stream);
-  return a.causal ? launch_stage_t<128, true>(a, stage, stream) : launch_stage_t<128, false>(a, stage, stream);
+    return a.causal ? launch_stage_c<64, true>(a, stage, stream) : launch_stage_c<64, false>(a, stage, stream);
+  return a.causal ? launch_stage_c<128, true>(a, stage, stream) : launch_stage_c<128, false>(a, stage, stream);
+}
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+  for (int stage = 0; stage < 2; ++stage) {
+    const cudaError_t e = launch_bwd_stage(a, stage, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace fa

@@ -38,6 +38,13 @@ struct FwdArgs {
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 
+// Additive mask on the scaled scores: bf16 element (b, h, i, j) at
+// p + b*sb + h*sh + i*sq + j (strides in elements, 0 broadcasts).
+struct BiasRef {
+  const uint16_t* p;
+  long long sb, sh, sq;
+};
+
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // bf16 maps as for the forward pass
   const void* o;                        // forward output, fp32 (or bf16 when o_bf16)
@@ -61,6 +68,7 @@ struct BwdArgs {
   int* status;
   unsigned long long wait_limit_ns;
   int stall_unit;                       // testing: CTA 0 skips one stage of its n-th unit (-1: never)
+  BiasRef bias;                         // additive mask of the forward pass (p null: none)
 };
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);

@@ -151,8 +151,7 @@ fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, int o_
  *           loads, others element by element (slower).  No +inf, no NaN.
  * Other arguments, results and errors as fa_fwd_ex; a null bias or an
  * invalid stride returns FA_ERR_INVALID_ARG, a bias at an odd address
- * FA_ERR_MISALIGNED.  The backward entry points do not take a bias:
- * gradients of a masked forward are outside this library.
+ * FA_ERR_MISALIGNED.  Gradients of a masked forward: fa_bwd_bias.
  */
 fa_status fa_fwd_bias(const void* q, const void* k, const void* v, void* o, int o_dtype, float* lse,
                       const void* bias, long long bias_stride_b, long long bias_stride_h, long long bias_stride_q,
@@ -238,6 +237,22 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
                     const void* dO, float* dq, float* dk, float* dv, float* workspace, const int* seqlens_q,
                     const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                     fa_stream_t stream);
+
+/* Gradients of fa_fwd_bias: fa_bwd_ex with the same additive mask (bias and
+ * its strides exactly as passed to the forward call that made o and lse).
+ * The mask enters only the recomputed probabilities,
+ * P_ij = exp(scale * q_i.k_j + bias_ij - LSE_i); it is a constant of the
+ * differentiation, so no gradient of the mask is formed.  Rows whose keys
+ * the mask hides entirely (LSE = -inf) get dQ = 0 and add nothing to dK, dV.
+ * Mask rows that start on a 16-byte boundary are read in 16-byte loads by the
+ * dQ kernel; the dK/dV kernel reads the mask down its columns, one 2-byte
+ * load per (query, key) per pass, coalesced over 32 consecutive keys.
+ * Errors as fa_bwd_ex and fa_fwd_bias. */
+fa_status fa_bwd_bias(const void* q, const void* k, const void* v, const void* o, int o_dtype, const float* lse,
+                      const void* dO, const void* bias, long long bias_stride_b, long long bias_stride_h,
+                      long long bias_stride_q, float* dq, float* dk, float* dv, float* workspace,
+                      const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
+                      int causal, fa_stream_t stream);
 
 /*
  * Largest B*H*N that fa_bwd_noalloc accepts: 2^20 rows, i.e. 4 MiB of fp32

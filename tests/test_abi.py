@@ -136,6 +136,18 @@ def test_bias_argument_errors(fa, bias, strides, expect):
     assert st == expect, fa.fa_status_string(st)
 
 
+@pytest.mark.parametrize("bias,strides,expect", [
+    (0, (0, 0, 16), 1),          # no bias
+    (FAKE + 1, (0, 0, 16), 3),   # odd address
+    (FAKE, (0, 0, 8), 1),        # query stride below Nk
+    (FAKE, (0, -8, 16), 1),      # negative stride
+])
+def test_backward_bias_argument_errors(fa, bias, strides, expect):
+    st = fa.fa_bwd_bias(FAKE, FAKE, FAKE, FAKE, 0, FAKE, FAKE, bias, *strides, FAKE, FAKE, FAKE, 0, 0, 0, 1, 1, 16,
+                        16, 64, 0.125, 0, 0)
+    assert st == expect, fa.fa_status_string(st)
+
+
 def test_status_strings(fa):
     seen = set()
     for code in range(7):

@@ -8,7 +8,7 @@ import torch
 import exact_tiled_attention_18_gb300 as fa
 import oracle
 from exact_tiled_attention_18_gb300 import workloads
-from tests.helpers import LSE_REL, O_MAX_ABS, O_MEAN_ABS, scale_for, to64
+from tests.helpers import GRAD_MAX_ABS, LSE_REL, O_MAX_ABS, O_MEAN_ABS, scale_for, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -126,3 +126,131 @@ def test_zero_bias_matches_unmasked_forward():
     b = fa.forward(q, k, v, causal=True)
     fa.sync_status()
     assert (a[0] - b[0]).abs().max() <= 2e-3 and (a[1] - b[1]).abs().max() <= 1e-5
+
+
+# ---------------------------------------------------------------- gradients
+
+def _check_grads(got, ref, what):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        g = g.cpu().double().numpy()
+        assert np.all(np.isfinite(g)), (what, name)
+        err = np.abs(g - r).max()
+        assert err <= GRAD_MAX_ABS, (what, name, err)
+
+
+def _grads(q, k, v, do, bias, scale, causal, lq=None, lk=None, o_dtype=None):
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.forward_bias(qc, kc, vc, bias, lq, lk, causal=causal, scale=scale, o_dtype=o_dtype)
+    g = fa.backward_bias(qc, kc, vc, o, lse, doc, bias, lq, lk, causal=causal, scale=scale)
+    fa.sync_status()
+    return tuple(t.cpu() for t in g)
+
+
+def _ref_grads(q, k, v, do, bias, scale, causal, sq=None, sk=None):
+    B, H, Nq, Nk = q.shape[0], q.shape[1], q.shape[2], k.shape[2]
+    bb = bias.expand(B, H, Nq, Nk).float().cpu().double().numpy()
+    if sq is None:
+        return oracle.backward(to64(q), to64(k), to64(v), to64(do), scale, causal, bb)[:3]
+    return oracle.backward_varlen(to64(q), to64(k), to64(v), to64(do), scale, causal, sq, sk, bb)[:3]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", [
+    (1, 2, 300, 300, 64, False),
+    (2, 1, 517, 517, 128, True),
+    (1, 2, 256, 640, 128, True),
+    (2, 2, 384, 384, 64, False),
+    (1, 1, 200, 129, 128, False),
+    (1, 2, 640, 256, 64, True),
+])
+def test_backward_random_bias(B, H, Nq, Nk, d, causal):
+    seed = 3 * Nq + Nk + d
+    g = workloads.make_decode_inputs(B, H, Nq, Nk, d, seed=seed)
+    do = workloads.randn_bf16((B, H, Nq, d), seed + 3)
+    bias = _bias((B, H, Nq, Nk), seed=seed + 4, hide=0.05)
+    scale = scale_for(d)
+    got = _grads(g["q"], g["k"], g["v"], do, bias, scale, causal)
+    _check_grads(got, _ref_grads(g["q"], g["k"], g["v"], do, bias, scale, causal), (B, H, Nq, Nk, d, causal))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_hidden_keys_and_rows(d):
+    B, H, N = 1, 2, 700
+    g = workloads.make_decode_inputs(B, H, N, N, d, seed=31 + d)
+    do = workloads.randn_bf16((B, H, N, d), 37 + d)
+    b = _bias((B, H, N, N), seed=41, hide=0.3).cpu()
+    b[0, 0, 5, :] = -float("inf")
+    b[0, 1, 10:20, :300] = -float("inf")
+    b[0, 1, 30, :690] = -float("inf")
+    b[0, 0, :, 650:] = -float("inf")   # keys no query sees: dK = dV = 0 there
+    bias = b.cuda()
+    scale = scale_for(d)
+    for causal in (False, True):
+        got = _grads(g["q"], g["k"], g["v"], do, bias, scale, causal)
+        _check_grads(got, _ref_grads(g["q"], g["k"], g["v"], do, bias, scale, causal), ("hidden", d, causal))
+        assert torch.all(got[0][0, 0, 5] == 0)
+        assert torch.all(got[1][0, 0, 650:] == 0) and torch.all(got[2][0, 0, 650:] == 0)
+
+
+@pytest.mark.parametrize("shape", ["shared", "per_head", "key_row"])
+def test_backward_broadcast_bias(shape):
+    B, H, Nq, Nk, d = 2, 3, 400, 400, 128
+    g = workloads.make_decode_inputs(B, H, Nq, Nk, d, seed=43)
+    do = workloads.randn_bf16((B, H, Nq, d), 47)
+    dims = {"shared": (1, 1, Nq, Nk), "per_head": (1, H, Nq, Nk), "key_row": (B, 1, 1, Nk)}[shape]
+    # key_row: a key-padding style mask (0 or -inf, with a little noise)
+    bias = _bias(dims, seed=53, gain=0.5 if shape == "key_row" else 2.0, hide=0.1 if shape == "key_row" else 0.0)
+    scale = scale_for(d)
+    got = _grads(g["q"], g["k"], g["v"], do, bias, scale, True)
+    _check_grads(got, _ref_grads(g["q"], g["k"], g["v"], do, bias, scale, True), shape)
+
+
+def test_backward_dominant_keys_within_rounding_bound():
+    """A per-key bias of N(0, 4) makes a few keys dominate every query, so
+    dV_j = sum_i P_ij dO_i sums hundreds of large terms (|dV| about 4x the
+    unmasked case).  The tensor-core product takes P in bf16 (unit roundoff
+    2^-8), which bounds the error of dV_jc by 2^-8 sum_i P_ij |dO_ic|; the
+    oracle gives that sum exactly as its dV for |dO|.  dQ and dK keep the
+    plain tolerance."""
+    B, H, Nq, Nk, d = 2, 3, 400, 400, 128
+    g = workloads.make_decode_inputs(B, H, Nq, Nk, d, seed=43)
+    do = workloads.randn_bf16((B, H, Nq, d), 47)
+    bias = _bias((B, 1, 1, Nk), seed=53, gain=2.0, hide=0.1)
+    scale = scale_for(d)
+    got = _grads(g["q"], g["k"], g["v"], do, bias, scale, True)
+    ref = _ref_grads(g["q"], g["k"], g["v"], do, bias, scale, True)
+    _check_grads(got[:2], ref[:2], "dominant keys")
+    mass = _ref_grads(g["q"], g["k"], g["v"], do.abs(), bias, scale, True)[2]
+    err = np.abs(got[2].double().numpy() - ref[2])
+    assert np.all(err <= GRAD_MAX_ABS + 2.0 ** -8 * mass), err.max()
+
+
+def test_backward_padded_batch_with_bias():
+    """Unequal and padded lengths, rows padded to a stride of 304 elements,
+    bf16 O from the forward; padding rows of the gradients are 0."""
+    B, H, Nq, Nk, d = 3, 2, 260, 300, 128
+    sq, sk = [260, 100, 7], [300, 299, 150]
+    g = workloads.make_decode_inputs(B, H, Nq, Nk, d, seed=59)
+    do = workloads.randn_bf16((B, H, Nq, d), 61)
+    bias = _bias((B, H, Nq, Nk), seed=67, hide=0.05, row_stride=304)
+    lq = torch.tensor(sq, dtype=torch.int32, device="cuda")
+    lk = torch.tensor(sk, dtype=torch.int32, device="cuda")
+    scale = scale_for(d)
+    got = _grads(g["q"], g["k"], g["v"], do, bias, scale, True, lq, lk, o_dtype=torch.bfloat16)
+    _check_grads(got, _ref_grads(g["q"], g["k"], g["v"], do, bias, scale, True, sq, sk), "padded bias")
+    dq, dk, dv = got
+    for b in range(B):
+        assert torch.all(dq[b, :, sq[b]:] == 0)
+        assert torch.all(dk[b, :, sk[b]:] == 0) and torch.all(dv[b, :, sk[b]:] == 0)
+
+
+def test_backward_zero_bias_matches_unmasked():
+    g = workloads.make_decode_inputs(1, 2, 500, 500, 128, seed=71)
+    q, k, v = (g[n].cuda() for n in ("q", "k", "v"))
+    do = workloads.randn_bf16((1, 2, 500, 128), 73).cuda()
+    zero = torch.zeros((1, 1, 1, 500), dtype=torch.bfloat16, device="cuda")
+    o, lse = fa.forward(q, k, v, causal=True)
+    a = fa.backward_bias(q, k, v, o, lse, do, zero, causal=True)
+    b = fa.backward(q, k, v, o, lse, do, causal=True)
+    fa.sync_status()
+    for x, y in zip(a, b):
+        assert (x - y).abs().max() <= 1e-4
