@@ -11,7 +11,7 @@
 //
 // Two kernels, in stream order:
 //   dq          one CTA per 128-query tile, sweeping its key tiles:
-//               S = Q K^T, dP = dO V^T, dS (hi + lo) in TMEM, dQ += dS K;
+//               S = Q K^T, dP = dO V^T, dS (bf16) in TMEM, dQ += dS K;
 //               a loader warp forms D' = rowsum(dO o O) one unit ahead, and
 //               the kernel corrects D' to the exact row term (see the
 //               kernel), so it runs before dkdv.
@@ -77,10 +77,13 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_
 
 // Two-term bf16 split of a pair of fp32 values: hi keeps the top 16 bits of
 // each value (truncation), lo is the exact remainder rounded to bf16, so
-// hi + lo carries about 16 significant bits.  dS feeds the dK and dQ
-// products this way: rows with large |q| (the long-context workload scales
-// every 64th query by 10) amplify a plain bf16 rounding of dS past the
-// gradient tolerance.
+// hi + lo carries about 16 significant bits.  dS^T feeds the dK product
+// this way: dK_j sums dS_ij q_i, and rows with large |q| (the long-context
+// workload scales every 64th query by 10) amplify a plain bf16 rounding of
+// dS past the gradient tolerance (dK error 0.155).  The dQ product sums
+// dS_ij k_j over keys of ordinary size and takes dS rounded to bf16 (dQ
+// error 8e-3 on that workload, against 2e-5 with the split, for one GEMM
+// fewer per tile).
 __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const uint32_t u0 = __float_as_uint(x0), u1 = __float_as_uint(x1);
   hi = __byte_perm(u0, u1, 0x7632);  // top halves of both: truncation to bf16
@@ -658,7 +661,7 @@ struct QLayout {
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
   // S [0,128): after use P (bf16) in each warpgroup's first 32 columns;
-  // dP [128,256): dS hi in each warpgroup's first 32 and dS lo in its last 32;
+  // dP [128,256): dS (bf16) in each warpgroup's first 32 columns;
   // dQ accumulator [256, 256+d); B = sum_j P_ij k_j accumulator [256+d, 256+2d).
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColB = 256 + D;
 };
@@ -824,8 +827,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             pk[c / 2] = pack_bf16x2(p0, p1);
           }
         };
-        // Phase 2: dS = P o (dP - D), its row sum, and its hi + lo split
-        auto dchunk = [&](const uint32_t (&pr)[32], const uint32_t (&dr)[32], uint32_t (&hk)[16], uint32_t (&lk)[16]) {
+        // Phase 2: dS = P o (dP - D), its row sum, and dS rounded to bf16
+        auto dchunk = [&](const uint32_t (&pr)[32], const uint32_t (&dr)[32], uint32_t (&hk)[16]) {
           uint64_t acc = f2_pack(0.f, 0.f);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
@@ -833,21 +836,21 @@ __global__ void __launch_bounds__(kQThreads, 1)
             const uint64_t ds01 = fmul2(f2_from(pr[c], pr[c + 1]), fsub2(f2_from(dr[c], dr[c + 1]), dd2));
             acc = fadd2(acc, ds01);
             f2_unpack(ds01, ds0, ds1);
-            split_bf16x2(ds0, ds1, hk[c / 2], lk[c / 2]);
+            hk[c / 2] = pack_bf16x2(ds0, ds1);
           }
           float a0, a1;
           f2_unpack(acc, a0, a1);
           dsum += a0 + a1;
         };
         // After use the warpgroup's slice holds P in S cols [64w, 64w+32) and
-        // dS hi and lo in dP cols [64w, 64w+32) and [64w+32, 64w+64); each
-        // store lands on columns this thread has already read.  P is published
+        // dS in dP cols [64w, 64w+32); each store lands on columns this
+        // thread has already read.  P is published
         // first so that B += P K, and then S of the next key tile, queue
         // behind dP in the tensor pipe.
         const uint32_t tS = tmem + lane_off + L::kColS + 64 * w;
         const uint32_t tD = tmem + lane_off + L::kColDP + 64 * w;
         {
-          uint32_t s0[32], s1[32], d0[32], d1[32], pk[16], hk[16], lk[16];
+          uint32_t s0[32], s1[32], d0[32], d1[32], pk[16], hk[16];
           tmem_ld32(tS, s0);
           tmem_ld32(tS + 32, s1);
           tmem_ld_wait();
@@ -868,12 +871,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
           tmem_ld32(tD, d0);
           tmem_ld32(tD + 32, d1);
           tmem_ld_wait();
-          dchunk(s0, d0, hk, lk);
+          dchunk(s0, d0, hk);
           tmem_st16(tD, hk);
-          tmem_st16(tD + 32, lk);
-          dchunk(s1, d1, hk, lk);
+          dchunk(s1, d1, hk);
           tmem_st16(tD + 16, hk);
-          tmem_st16(tD + 48, lk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -1101,11 +1102,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
         issue_dp(kv_k(kvpos) + kTileUnits);
         // Per key tile jt: B += P K once P is stored; then S of tile jt+1,
         // which overwrites P(jt) only after B(jt) has read it (the tensor
-        // pipe runs in issue order); then dQ += dS K (hi and lo, both in the
-        // dP columns); then dP of tile jt+1, behind dQ(jt).  M = 128 queries,
-        // N = d, K = 128 keys, K tile MN-major; the warpgroup w's P sits in S
-        // columns [64 w, 64 w + 32), its dS hi and lo in dP columns
-        // [64 w, 64 w + 32) and [64 w + 32, 64 w + 64).
+        // pipe runs in issue order); then dQ += dS K (dS in the dP columns);
+        // then dP of tile jt+1, behind dQ(jt).  M = 128 queries, N = d,
+        // K = 128 keys, K tile MN-major; the warpgroup w's P sits in S
+        // columns [64 w, 64 w + 32), its dS in dP columns [64 w, 64 w + 32).
         for (int jt = 0; jt < nk; ++jt) {
           const uint32_t s = kvpos % S;
           const uint64_t kmn = kv_mn(kvpos);
@@ -1134,12 +1134,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
             umma_ts(tmem + L::kColDQ, tmem + L::kColDP + acol, kmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
                     (jt > 0 || ks > 0) ? 1u : 0u);
-          }
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {  // dS lo part
-            const uint32_t acol = 32 + 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDQ, tmem + L::kColDP + acol, kmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
-                    1u);
           }
           umma_commit(BAR(L::KV_EMPTY + s));
           ++kvpos;

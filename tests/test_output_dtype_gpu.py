@@ -56,7 +56,9 @@ def test_bf16_output_padded_batch_matches_oracle():
 @pytest.mark.parametrize("causal", [False, True])
 def test_backward_from_bf16_output(causal):
     """The row term is corrected to the recomputed probabilities, so the
-    gradients from a bf16 O match the oracle and the fp32-O gradients."""
+    gradients from a bf16 O match the oracle and the fp32-O gradients: dK and
+    dV to 1e-3; dQ, which takes dS rounded to bf16 (whose rounding differs
+    between the two runs, whose D' differ), within the gradient tolerance."""
     B, H, N, d = 1, 2, 640, 128
     inp = workloads.make_inputs(B, H, N, d, seed=44 + causal, with_grad=True, boost_every=64, boost=10.0)
     scale = scale_for(d)
@@ -70,4 +72,4 @@ def test_backward_from_bf16_output(causal):
     for name, a, b, r in zip(("dQ", "dK", "dV"), g16, g32, ref[:3]):
         a64 = a.cpu().double().numpy()
         assert np.abs(a64 - r).max() <= GRAD_MAX_ABS, name
-        assert (a - b).abs().max() <= 1e-3, name
+        assert (a - b).abs().max() <= (GRAD_MAX_ABS if name == "dQ" else 1e-3), name
