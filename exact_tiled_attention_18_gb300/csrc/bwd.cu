@@ -791,7 +791,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
       for (int jt = 0; jt < nk; ++jt) {
         // the mask of the warpgroup's 64 keys, fetched before the wait
         uint32_t bb0[BIAS ? 16 : 1], bb1[BIAS ? 16 : 1];
-        if constexpr (BIAS) load_bias_row(brow, bvec, jt * kTileRows + 64 * w, geom.nk, bb0, bb1);
+        if constexpr (BIAS) {
+          load_bias_row(brow, bvec, jt * kTileRows + 64 * w, geom.nk, bb0, bb1);
+          // the next key tile's 128 bytes of this row towards L2
+          const int knext = (jt + 1) * kTileRows + 64 * w;
+          if (brow && jt + 1 < nk && knext + 64 <= geom.nk) prefetch_l2(brow + knext);
+        }
         // P needs only S: dP may still be in the tensor pipe
         const uint32_t sdp_parity = sn & 1;
         ok = warp_wait(BAR(L::S_FULL), sdp_parity, wc, SITE_Q_EW_S, unit);

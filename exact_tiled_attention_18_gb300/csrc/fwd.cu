@@ -241,6 +241,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (bvec && col0 + kTileRows <= geom.nk) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) bq[i] = __ldg(reinterpret_cast<const uint4*>(brow + col0) + i);
+            // the row's next 256 bytes towards L2, a tile ahead of their use
+            if (j + 1 < nt && col0 + 2 * kTileRows <= geom.nk) {
+              prefetch_l2(brow + col0 + kTileRows);
+              prefetch_l2(brow + col0 + kTileRows + 64);
+            }
           } else {
             // a row that is not 16-byte aligned, the tile past the end of
             // the bias rows, or a padding row: element loads; keys from Nk on

@@ -116,6 +116,11 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
 
 // ---------------------------------------------------------------------- TMA
 
+// Bring the 128-byte line holding p into L2 (a hint: no fault, no result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
