@@ -44,6 +44,29 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 L2_BYTES = 126 * 1024 * 1024
 
 
+# Additive masks for --mask: bf16, seeded N(0,1) entries (the key-padding
+# style one also hides 10% of the keys), shape broadcast to [B, H, N, N].
+MASKS = {
+    "none": None,
+    "key_row": "one row of key biases per sequence [B,1,1,N] (query stride 0), 10% of keys hidden",
+    "shared": "one N x N mask shared by every head [1,1,N,N]",
+    "per_head": "one N x N mask per head [1,H,N,N]",
+}
+
+
+def make_mask(kind, B, H, N, device, seed):
+    import torch
+    if kind == "none":
+        return None
+    shape = {"key_row": (B, 1, 1, N), "shared": (1, 1, N, N), "per_head": (1, H, N, N)}[kind]
+    g = torch.Generator(device=device)
+    g.manual_seed(1000 + seed)
+    m = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if kind == "key_row":
+        m[torch.rand(shape, generator=g, device=device) < 0.1] = float("-inf")
+    return m.to(torch.bfloat16)
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -52,6 +75,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--fwd-only", action="store_true", help="time the forward pass alone")
+    p.add_argument("--mask", choices=list(MASKS), default="none",
+                   help="general additive mask (fa_fwd_bias / fa_bwd_bias) on the training workloads")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--e2e-chunks", type=int, default=4,
                    help="batch chunks in flight in the end-to-end pipeline (copies overlap kernels)")
@@ -260,18 +285,28 @@ def run_ours(args):
         ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N) // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     launches_per_step = 1 + (2 if do_bwd else 0)
+    mask = make_mask(args.mask, B, H, N, device, rank)
 
     ev = []
-    nev = 4 if do_bwd else 2
+    # with a mask the backward is one fa_bwd_bias call (its two kernels timed together)
+    nev = (4 if mask is None else 3) if do_bwd else 2
 
     def step(record):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(nev)] if record else None
         if record:
             e[0].record(stream)
-        fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=(o, lse))
+        if mask is None:
+            fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=(o, lse))
+        else:
+            fa.forward_bias(q, k, v, mask, causal=w.causal, scale=w.scale, out=(o, lse))
         if record:
             e[1].record(stream)
-        if do_bwd:
+        if do_bwd and mask is not None:
+            fa.backward_bias(q, k, v, o, lse, dout, mask, causal=w.causal, scale=w.scale, workspace=ws,
+                             out=(dq, dk, dv))
+            if record:
+                e[2].record(stream)
+        elif do_bwd:
             # fa_bwd's two kernels, one C call each so each can be timed
             for stage in range(2):
                 fa.backward_stage(stage, q, k, v, o, lse, dout, dq, dk, dv, ws, causal=w.causal, scale=w.scale)
@@ -311,7 +346,7 @@ def run_ours(args):
     # end to end through the public API: pinned host inputs in, results out,
     # every step; the batch moves in chunks so that copies overlap kernels
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and mask is None:
         from exact_tiled_attention_18_gb300.pipeline import HostStepPipeline
         names = ["q", "k", "v"] + (["do"] if do_bwd else [])
         host_in = {n: inp[n].pin_memory() for n in names}
@@ -340,7 +375,7 @@ def run_ours(args):
                "chunks_in_flight": chunks}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and mask is None:
         tf, heads, secs = oracle_sample(w, 0, 10.0)
         cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
                "sample": f"{heads} whole head(s) of the workload (N={w.N}, d={w.d}, causal={w.causal}), "
@@ -357,7 +392,9 @@ def run_ours(args):
     # dK), each 2*N^2*d per head, halved under the causal mask.
     gemm = w.fwd_flops() / 2
     kernels = [("fwd_kernel", fwd_ms, "tensor", 2 * gemm)]
-    if do_bwd:
+    if do_bwd and mask is not None:
+        kernels += [("dq_kernel+dkdv_kernel", kern_ms[1], "tensor", 7 * gemm)]
+    elif do_bwd:
         kernels += [("dq_kernel", kern_ms[1], "tensor", 3 * gemm),
                     ("dkdv_kernel", kern_ms[2], "tensor", 4 * gemm)]
     name, ms, bound, work = max(kernels, key=lambda t: t[1])
@@ -370,7 +407,7 @@ def run_ours(args):
     roofline = {"bound": bound, "kernel": name, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                 "algorithmic_per_launch": work, "ms_per_launch": round(ms, 4),
-                "traffic": ncu_traffic(name, w.name)}
+                "traffic": ncu_traffic(name, w.name) if mask is None else None}
     if bound == "tensor":
         roofline["frac_of_burst_peak"] = round(achieved / burst, 4)
     per_kernel = {n: {"ms": round(t, 4),
@@ -393,7 +430,8 @@ def run_ours(args):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "step": "fwd+bwd" if do_bwd else "fwd",
                    "l2": f"inputs {3 * w.B * w.H * w.N * w.d * 2 / 2**20:.0f} MiB of Q,K,V > L2; no flush",
-                   "parallelism": f"heads independent; {world} rank(s) x own batch, no collective"},
+                   "parallelism": f"heads independent; {world} rank(s) x own batch, no collective",
+                   **({"mask": MASKS[args.mask]} if mask is not None else {})},
         "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fwd_tflops, 2),
                 "frac_of_sustained": round(fwd_tflops / sustained, 4), "frac_of_burst": round(fwd_tflops / burst, 4)},
         "bwd": ({"ms": round(bwd_ms, 4), "tflops": round(bwd_tflops, 2),
@@ -402,6 +440,8 @@ def run_ours(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        **({"note": "with a mask: no e2e (the host pipeline carries no mask), no cpu_baseline, no ncu traffic "
+                    "(the profiles cover the unmasked kernels)"} if mask is not None else {}),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -630,6 +670,8 @@ def run_reference_decode(args):
 def main(argv=None):
     args = parse_args(argv)
     from exact_tiled_attention_18_gb300 import workloads
+    if args.mask != "none" and (args.impl == "reference" or args.workload in workloads.DECODE_WORKLOADS):
+        raise SystemExit("--mask applies to our arm on the training workloads only")
     if args.impl == "reference":
         line = run_reference(args)
     elif args.workload in workloads.DECODE_WORKLOADS:

@@ -105,6 +105,33 @@ def test_backward_full_size_whole_heads(name, heads):
         check_grads(got, (rq, rk, rv), f"{name} head {(b, h)}")
 
 
+def test_backward_masked_positions_do_not_leak():
+    """Extreme values at causally masked key/value positions leave the
+    gradients of the rows that cannot see them unchanged: with keys from 160
+    on set to +1e4 and their values to -1e4, dQ and the row term D of
+    queries 0..159 stay bit for bit the same (160 is a warp boundary)."""
+    B, H, N, d = 1, 2, 300, 64
+    inp = workloads.make_inputs(B, H, N, d, seed=13, with_grad=True)
+    scale = scale_for(d)
+
+    def run(x):
+        q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+        o, lse = fa.forward(q, k, v, causal=True, scale=scale)
+        ws = torch.empty(B * H * N, dtype=torch.float32, device="cuda")
+        dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=True, scale=scale, workspace=ws)
+        fa.sync_status()
+        return dq.cpu(), ws.cpu().reshape(B, H, N)
+
+    dq1, d1 = run(inp)
+    poisoned = {n: t.clone() for n, t in inp.items()}
+    poisoned["k"][:, :, 160:, :] = 1e4
+    poisoned["v"][:, :, 160:, :] = -1e4
+    dq2, d2 = run(poisoned)
+    assert torch.isfinite(dq2).all()
+    assert torch.equal(dq1[:, :, :160], dq2[:, :, :160])
+    assert torch.equal(d1[:, :, :160], d2[:, :, :160])
+
+
 def test_stages_equal_fa_bwd():
     """fa_bwd_stage 0, 1 in order is exactly fa_bwd."""
     inp = workloads.make_inputs(2, 2, 300, 128, seed=31, with_grad=True)
