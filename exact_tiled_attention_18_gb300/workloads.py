@@ -140,6 +140,21 @@ def make_inputs(B: int, H: int, N: int, d: int, seed: int = 0, with_grad: bool =
     return out
 
 
+def make_fp8_inputs(B: int, H: int, N: int, d: int, seed: int = 0) -> dict:
+    """Seeded N(0,1) q, k, v rounded to FP8 E4M3 by torch's float32 ->
+    float8_e4m3fn cast, as uint8 bit patterns: q, k, v [B, H, N, d] and vt,
+    v transposed to [B, H, d, N] (the layout the FP8 forward reads V in)."""
+    g = torch.Generator().manual_seed(seed)
+    q, k, v = (torch.randn((B, H, N, d), generator=g) for _ in range(3))
+    q8, k8, v8 = (t.to(torch.float8_e4m3fn).view(torch.uint8) for t in (q, k, v))
+    return {"q": q8, "k": k8, "v": v8, "vt": v8.transpose(-1, -2).contiguous()}
+
+
+def fp8_values(t: torch.Tensor) -> torch.Tensor:
+    """float32 values of E4M3 bit patterns held as uint8."""
+    return t.view(torch.float8_e4m3fn).to(torch.float32)
+
+
 def workload_inputs(w: Workload, seed: int = 0) -> dict:
     return make_inputs(w.B, w.H, w.N, w.d, seed=seed, with_grad=w.backward,
                        boost_every=w.boost_every, boost=w.boost)

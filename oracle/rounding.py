@@ -19,6 +19,10 @@ is the one the recomputation backward rounds: dS formed with the row term
 of the rounded forward output, whose difference from the exact row term is
 then taken out again in fp64.
 
+The FP8 forward takes its inputs as E4M3 values and rounds P to E4M3 before
+O = P V; ``forward(..., p_round=round_e4m3)`` is its companion, the plain
+definition applied to those input values its parity reference.
+
 A kernel result much closer to this prediction than to the definition shows
 that its error is the prescribed rounding rather than a defect.  The kernels
 round P relative to a running reference maximum that may lag the row maximum
@@ -32,7 +36,7 @@ import numpy as np
 
 from . import attention
 
-__all__ = ["round_bf16", "forward_head", "forward", "backward_head", "backward"]
+__all__ = ["round_bf16", "round_e4m3", "forward_head", "forward", "backward_head", "backward"]
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:
@@ -46,22 +50,42 @@ def round_bf16(x: np.ndarray) -> np.ndarray:
     return u.astype(np.uint32).view(np.float32).astype(np.float64).reshape(np.shape(x))
 
 
-def forward_head(q, k, v, scale, causal, bias=None):
-    """attention.forward_head with the weights rounded to bf16 before the
-    product with V (the normaliser l is the sum of the unrounded weights)."""
+def round_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest FP8 E4M3 value (ties to even), saturating at
+    +-448, returned as float64.
+
+    E4M3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinities.
+    Normal values 1.mmm * 2^e for e >= -6 (largest 1.75 * 2^8 = 448);
+    below 2^-6 the subnormals 0.mmm * 2^-6, spacing 2^-9.  So a value in the
+    binade [2^e, 2^(e+1)) rounds on a grid of spacing 2^(e-3), with e held
+    at -6 for the subnormal range."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(a)                      # a = f * 2^e, f in [0.5, 1): binade exponent e - 1
+    e = np.maximum(e.astype(np.float64) - 1.0, -6.0)
+    step = np.exp2(e - 3.0)
+    r = np.minimum(np.round(a / step) * step, 448.0)   # np.round: half to even
+    return np.copysign(r, x)
+
+
+def forward_head(q, k, v, scale, causal, bias=None, p_round=None):
+    """attention.forward_head with the weights rounded before the product
+    with V (the normaliser l is the sum of the unrounded weights): to bf16
+    by default, or by ``p_round`` (round_e4m3 for the FP8 forward)."""
+    p_round = round_bf16 if p_round is None else p_round
     s, ok = attention._masked_scores(q, k, scale, causal, bias)
     has_key = ok.any(axis=1)
     m = np.where(has_key, s.max(axis=1, initial=-np.inf), 0.0)
     w = np.where(ok, np.exp(s - m[:, None]), 0.0)
     l = w.sum(axis=1)
     safe_l = np.where(has_key, l, 1.0)
-    o = (round_bf16(w) @ v) / safe_l[:, None]
+    o = (p_round(w) @ v) / safe_l[:, None]
     o[~has_key] = 0.0
     lse = np.where(has_key, m + np.log(safe_l), -np.inf)
     return o, lse
 
 
-def forward(q, k, v, scale, causal, bias=None):
+def forward(q, k, v, scale, causal, bias=None, p_round=None):
     """forward_head over [B, H, N, d] arrays; returns (O, LSE)."""
     b, h, nq, _ = q.shape
     o = np.empty((b, h, nq, v.shape[-1]), dtype=np.float64)
@@ -69,7 +93,7 @@ def forward(q, k, v, scale, causal, bias=None):
     for bi in range(b):
         for hi in range(h):
             o[bi, hi], lse[bi, hi] = forward_head(q[bi, hi], k[bi, hi], v[bi, hi], scale, causal,
-                                                  None if bias is None else bias[bi, hi])
+                                                  None if bias is None else bias[bi, hi], p_round)
     return o, lse
 
 

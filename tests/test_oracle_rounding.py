@@ -75,3 +75,39 @@ def test_backward_rounding_error_within_its_bound():
         bound_q = 2.0 ** -8 * scale * (np.abs(ds_out) @ np.abs(k[0, 0]))
         assert np.all(np.abs(eq[0, 0] - dq[0, 0]) <= bound_q + 1e-13) and np.abs(eq - dq).max() > 0
         assert np.max(np.abs(ek - dk)) < 1e-13 and np.max(np.abs(ed - dd)) < 1e-13
+
+
+def test_round_e4m3_matches_torch_cast():
+    """Against torch's float32 -> float8_e4m3fn cast over the E4M3 range:
+    every representable value, the midpoints between neighbours (ties to
+    even), subnormals, and random values."""
+    grid = np.unique(torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float32).numpy())
+    grid = grid[np.isfinite(grid)]
+    mids = (grid[:-1] + grid[1:]) / 2
+    rng = np.random.default_rng(5)
+    rand = (rng.standard_normal(20000) * 2.0 ** rng.integers(-12, 9, 20000)).astype(np.float32)
+    x = np.concatenate([grid, mids, rand]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    ref = torch.from_numpy(x.copy()).to(torch.float8_e4m3fn).to(torch.float32).numpy().astype(np.float64)
+    assert np.array_equal(rounding.round_e4m3(x.astype(np.float64)), ref)
+    assert rounding.round_e4m3(np.array([500.0, -1e6]))[0] == 448 and rounding.round_e4m3(np.array([-1e6]))[0] == -448
+
+
+def test_fp8_forward_error_within_its_bound():
+    """|e4m3(w) - w| <= 2^-4 w + 2^-10 (relative half-spacing of 3 mantissa
+    bits; half the subnormal spacing), so with the weights w_ij = P_ij e^(LSE_i
+    - m_i) <= 1, |dO_i| <= 2^-4 sum_j P_ij |v_j| + 2^-10 e^(m_i - LSE_i) sum_j |v_j|."""
+    q, k, v, _ = _case(1, 2, 64, 16, 6, boost=True)
+    q, k, v = (rounding.round_e4m3(t) for t in (q, k, v))
+    for causal in (False, True):
+        o, lse = oracle.forward(q, k, v, 0.5, causal)
+        oe, lsee = rounding.forward(q, k, v, 0.5, causal, p_round=rounding.round_e4m3)
+        mass, _ = oracle.forward(q, k, np.abs(v), 0.5, causal)
+        s = 0.5 * np.einsum("bhid,bhjd->bhij", q, k)
+        ok = oracle.eligible(64, 64, causal)
+        m = np.where(ok, s, -np.inf).max(axis=-1)
+        vsum = np.einsum("ij,bhjd->bhid", ok.astype(np.float64), np.abs(v))
+        bound = 2.0 ** -4 * mass + 2.0 ** -10 * np.exp(m - lse)[..., None] * vsum
+        err = np.abs(oe - o)
+        assert np.all(err <= bound + 1e-15) and err.max() > 1e-3
+        assert np.array_equal(lse, lsee)
