@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_bias.argtypes = [vp, vp, vp, vp, i, vp, vp, vp, ll, ll, ll, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
                                   i, vp]
         L.fa_bwd_bias.restype = st
+        L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_fwd_fp8.restype = st
         L.fa_fwd_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_fwd_decode.restype = st
         L.fa_fwd_decode_workspace_bytes.argtypes = [i, i, i, i, i]
@@ -133,6 +135,11 @@ def fa_bwd_bias(q: int, k: int, v: int, o: int, o_dtype: int, lse: int, do: int,
                 stream: int) -> int:
     return lib().fa_bwd_bias(q, k, v, o, o_dtype, lse, do, bias, bias_stride_b, bias_stride_h, bias_stride_q, dq, dk,
                              dv, workspace, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream)
+
+
+def fa_fwd_fp8(q8: int, k8: int, vt8: int, o: int, lse: int, B: int, H: int, N: int, d: int, scale: float,
+               causal: int, stream: int) -> int:
+    return lib().fa_fwd_fp8(q8, k8, vt8, o, lse, B, H, N, d, scale, causal, stream)
 
 
 def fa_fwd_decode(q: int, k: int, v: int, o: int, lse: int, seqlens_q: int, seqlens_k: int, workspace: int, B: int,
@@ -320,6 +327,29 @@ def forward_bias(q, k, v, bias, seqlens_q=None, seqlens_k=None, causal: bool = F
                                       seqlens_q.data_ptr() if seqlens_q is not None else 0,
                                       seqlens_k.data_ptr() if seqlens_k is not None else 0,
                                       B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    return o, lse
+
+
+def forward_fp8(q8, k8, vt8, causal: bool = False, scale: float | None = None, out=None):
+    """O, LSE through fa_fwd_fp8: q8, k8 [B,H,N,128] and vt8 (V transposed)
+    [B,H,128,N], E4M3 CUDA tensors (torch.float8_e4m3fn, or uint8 holding
+    the bit patterns), contiguous; O fp32."""
+    import torch
+    for t in (q8, k8, vt8):
+        if not t.is_cuda or t.dtype not in (torch.uint8, torch.float8_e4m3fn) or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q8, k8, vt8 must be contiguous 4-D E4M3 (or uint8) CUDA tensors")
+    B, H, N, d = q8.shape
+    if k8.shape != q8.shape or vt8.shape != (B, H, d, N):
+        raise ValueError("k8 must be [B, H, N, d] and vt8 [B, H, d, N]")
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    if out is None:
+        o = torch.empty((B, H, N, d), dtype=torch.float32, device=q8.device)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    else:
+        o, lse = out
+    _check("fa_fwd_fp8", fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                    B, H, N, d, scale, int(bool(causal)), _stream_handle(q8.device)))
     return o, lse
 
 

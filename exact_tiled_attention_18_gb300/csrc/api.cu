@@ -78,6 +78,21 @@ bool encode_bf16_map(CUtensorMap* m, const void* base, int heads, int n, int d, 
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over one-byte elements [heads][rows][inner], 128 x 128 boxes with
+// the 128-byte swizzle (one 128-byte row of the box per matrix row).
+bool encode_u8_map(CUtensorMap* m, const void* base, int heads, int rows, int inner) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows) * inner};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(fa::kTileRows), 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 unsigned long long wait_limit_ns() {
   static unsigned long long v = []() -> unsigned long long {
     const char* s = std::getenv("FA_WAIT_LIMIT_MS");
@@ -311,6 +326,39 @@ size_t fa_fwd_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
   if (B < 1 || H < 1 || Nq < 1 || Nq > FA_DECODE_MAX_Q || Nk < 1 || (d != 64 && d != 128)) return 0;
   if (static_cast<long long>(B) * H * Nk >= (1LL << 31)) return 0;
   return static_cast<size_t>(B) * H * decode_max_splits(Nk) * Nq * (d + 1) * sizeof(float);
+}
+
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, float* o, float* lse, int B, int H, int N,
+                     int d, float scale, int causal, fa_stream_t stream) {
+  if (!q8 || !k8 || !vt8 || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, N, d, causal);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED_D;
+  if (N % 16 != 0) return FA_ERR_INVALID_ARG;  // rows of v^T: whole 16-byte groups
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q8, 16) || !aligned(k8, 16) || !aligned(vt8, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA_ERR_MISALIGNED;
+  DeviceInfo di;
+  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
+  const int heads = B * H;
+  fa::FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_u8_map(&a.tm_q, q8, heads, N, d) || !encode_u8_map(&a.tm_k, k8, heads, N, d) ||
+      !encode_u8_map(&a.tm_v, vt8, heads, d, N))
+    return FA_ERR_LAUNCH;
+  a.o = o;
+  a.lse = lse;
+  a.geom.nq = N;
+  a.geom.nk = N;
+  a.geom.heads_per_batch = H;
+  a.d = d;
+  a.causal = causal;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.sched = make_sched(heads, N, d, causal, di.sms, 0, fa::kUnitRows, 1, N);
+  a.status = di.status;
+  a.wait_limit_ns = wait_limit_ns();
+  a.stall_unit = test_stall_unit();
+  return fa::launch_fwd_fp8(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 fa_status fa_fwd_decode(const void* q, const void* k, const void* v, float* o, float* lse, const int* seqlens_q,

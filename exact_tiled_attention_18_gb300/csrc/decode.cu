@@ -35,7 +35,7 @@ constexpr int kDecThreads = 32 * (kDecConsumerWarps + 1);
 constexpr float kDecTau = 8.f;  // lazy rescale threshold (log2 units), as in the prefill kernel
 constexpr float kDecLn2 = 0.6931471805599453f;
 
-enum DecSite : int { SITE_DEC_EMPTY = 31, SITE_DEC_FULL = 32 };
+enum DecSite : int { SITE_DEC_EMPTY = 35, SITE_DEC_FULL = 36 };
 
 // Resident CTAs per SM: two, except with 8 query rows, whose registers need
 // the whole file; that case runs one CTA per SM with twice the ring, so the

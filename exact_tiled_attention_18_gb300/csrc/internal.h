@@ -73,6 +73,10 @@ struct BwdArgs {
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 
+// FP8 forward (E4M3 q, k and v^T, d = 128, square): tm_q, tm_k over
+// [B*H][N][128] bytes, tm_v over v^T [B*H][128][N] bytes; o fp32.
+cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream);
+
 struct DecArgs {
   CUtensorMap tm_k, tm_v;  // 3-D maps over [B*H][Nk][d] bf16, box 64 x 64 x 1, 128-byte swizzle
   const uint16_t* q;       // [B*H][Nq][d] bf16

@@ -159,6 +159,24 @@ fa_status fa_fwd_bias(const void* q, const void* k, const void* v, void* o, int 
                       int causal, fa_stream_t stream);
 
 /*
+ * FP8 forward: fa_fwd with E4M3 inputs ("FlashAttention 1, 2 & 3", section on
+ * FlashAttention-3: FP8 on the tensor cores).  q8, k8: [B][H][N][128] E4M3
+ * (one byte each); vt8: V transposed, [B][H][128][N] E4M3; o fp32
+ * [B][H][N][128], lse fp32 [B][H][N], as fa_fwd.  Scores and both products
+ * accumulate in fp32 from the E4M3 values as given (descale factors of q and
+ * k fold into `scale`; one of v multiplies O, which the caller applies);
+ * the probabilities P are rounded to E4M3 before O = P V, so O carries an
+ * error of up to 2^-4 sum_j P_ij |v_j| plus a subnormal term against the
+ * exact result on the same inputs; LSE does not (it sums the unrounded P).
+ * d must be 128 (else FA_ERR_UNSUPPORTED_D); N a multiple of 16 (rows of
+ * vt8 are whole 16-byte groups; else FA_ERR_INVALID_ARG); square sequences,
+ * causal or not.  All pointers 16-byte aligned (lse 4).  Errors and
+ * asynchrony as fa_fwd.
+ */
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, float* o, float* lse, int B, int H, int N,
+                     int d, float scale, int causal, fa_stream_t stream);
+
+/*
  * Decode-shaped forward: 1 <= Nq <= FA_DECODE_MAX_Q query rows per head
  * against a long key/value history.  Computes exactly what fa_fwd_varlen
  * computes for the same arguments (same layouts, lengths, bottom-right causal
@@ -314,6 +332,8 @@ fa_status fa_sync_status(fa_stream_t stream);
 /*
  * Details of the last device-side failure read by fa_sync_status():
  * out[0] status code, out[1] wait site, out[2] block index, out[3] work unit.
+ * Wait sites: 1-7 forward, 11-20 dK/dV, 21-32 dQ, 35-36 decode, 41-47 FP8
+ * forward (each kernel's source names them).
  * Returns FA_OK, or FA_ERR_INVALID_ARG if out is NULL.
  */
 fa_status fa_last_failure(int out[4]);

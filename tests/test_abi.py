@@ -148,6 +148,17 @@ def test_backward_bias_argument_errors(fa, bias, strides, expect):
     assert st == expect, fa.fa_status_string(st)
 
 
+@pytest.mark.parametrize("ptrs,dims,expect", [
+    ((0, FAKE, FAKE), (1, 1, 128, 128), 1),        # null pointer
+    ((FAKE, FAKE, FAKE), (1, 1, 128, 64), 2),      # d must be 128
+    ((FAKE, FAKE, FAKE), (1, 1, 100, 128), 1),     # N not a multiple of 16
+    ((FAKE + 1, FAKE, FAKE), (1, 1, 128, 128), 3),  # misaligned
+])
+def test_fp8_argument_errors(fa, ptrs, dims, expect):
+    st = fa.fa_fwd_fp8(*ptrs, FAKE, FAKE, *dims, 0.125, 0, 0)
+    assert st == expect, fa.fa_status_string(st)
+
+
 def test_status_strings(fa):
     seen = set()
     for code in range(7):
