@@ -75,6 +75,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--fwd-only", action="store_true", help="time the forward pass alone")
+    p.add_argument("--fp8", action="store_true",
+                   help="the forward alone through fa_fwd_fp8 on E4M3 inputs of the workload's shape (d = 128)")
     p.add_argument("--mask", choices=list(MASKS), default="none",
                    help="general additive mask (fa_fwd_bias / fa_bwd_bias) on the training workloads")
     p.add_argument("--e2e-steps", type=int, default=10)
@@ -101,6 +103,7 @@ KERNEL_SOURCES = {
     "dq_kernel": ["bwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
     "dkdv_kernel": ["bwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
     "decode_kernel": ["decode.cu", "geom.cuh", "ptx.cuh", "internal.h"],
+    "fwd_fp8_kernel": ["fwd_fp8.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
 }
 
 
@@ -270,7 +273,7 @@ def run_ours(args):
     device = torch.device("cuda", local)
     dist = init_dist(rank, world, "nccl")
     w = workloads.WORKLOADS[args.workload]
-    do_bwd = w.backward and not args.fwd_only
+    do_bwd = w.backward and not args.fwd_only and not args.fp8
     peaks, peak_kind = load_peaks()
 
     # inputs resident in HBM before the timed region (each rank its own batch)
@@ -286,6 +289,9 @@ def run_ours(args):
     stream = torch.cuda.current_stream(device)
     launches_per_step = 1 + (2 if do_bwd else 0)
     mask = make_mask(args.mask, B, H, N, device, rank)
+    if args.fp8:
+        x8 = workloads.make_fp8_inputs(B, H, N, d, seed=rank)
+        q8, k8, vt8 = (x8[n].to(device) for n in ("q", "k", "vt"))
 
     ev = []
     # with a mask the backward is one fa_bwd_bias call (its two kernels timed together)
@@ -295,7 +301,9 @@ def run_ours(args):
         e = [torch.cuda.Event(enable_timing=True) for _ in range(nev)] if record else None
         if record:
             e[0].record(stream)
-        if mask is None:
+        if args.fp8:
+            fa.forward_fp8(q8, k8, vt8, causal=w.causal, scale=w.scale, out=(o, lse))
+        elif mask is None:
             fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=(o, lse))
         else:
             fa.forward_bias(q, k, v, mask, causal=w.causal, scale=w.scale, out=(o, lse))
@@ -346,7 +354,7 @@ def run_ours(args):
     # end to end through the public API: pinned host inputs in, results out,
     # every step; the batch moves in chunks so that copies overlap kernels
     e2e = None
-    if args.e2e_steps > 0 and mask is None:
+    if args.e2e_steps > 0 and mask is None and not args.fp8:
         from exact_tiled_attention_18_gb300.pipeline import HostStepPipeline
         names = ["q", "k", "v"] + (["do"] if do_bwd else [])
         host_in = {n: inp[n].pin_memory() for n in names}
@@ -375,7 +383,7 @@ def run_ours(args):
                "chunks_in_flight": chunks}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and mask is None:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and mask is None and not args.fp8:
         tf, heads, secs = oracle_sample(w, 0, 10.0)
         cpu = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
                "sample": f"{heads} whole head(s) of the workload (N={w.N}, d={w.d}, causal={w.causal}), "
@@ -383,15 +391,16 @@ def run_ours(args):
 
     if rank != 0:
         return None
-    sustained = peaks["bf16_tflops_sustained"]
-    burst = peaks["bf16_tflops"]
+    # an E4M3 contraction takes the bf16 peaks x the nominal dense E4M3/bf16 ratio (4.5 / 2.25)
+    sustained = peaks["bf16_tflops_sustained"] * (2 if args.fp8 else 1)
+    burst = peaks["bf16_tflops"] * (2 if args.fp8 else 1)
     fwd_tflops = w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
     bwd_tflops = w.bwd_flops() / (bwd_ms * 1e-3) / 1e12 if do_bwd else None
     # Algorithmic work per launch of each kernel (one launch covers the whole
     # batch): forward 2 GEMMs (S, PV); dQ 3 (S, dP, dQ); dK/dV 4 (S, dP, dV,
     # dK), each 2*N^2*d per head, halved under the causal mask.
     gemm = w.fwd_flops() / 2
-    kernels = [("fwd_kernel", fwd_ms, "tensor", 2 * gemm)]
+    kernels = [("fwd_fp8_kernel" if args.fp8 else "fwd_kernel", fwd_ms, "tensor", 2 * gemm)]
     if do_bwd and mask is not None:
         kernels += [("dq_kernel+dkdv_kernel", kern_ms[1], "tensor", 7 * gemm)]
     elif do_bwd:
@@ -400,7 +409,8 @@ def run_ours(args):
     name, ms, bound, work = max(kernels, key=lambda t: t[1])
     if bound == "tensor":
         achieved, peak, unit = work / (ms * 1e-3) / 1e12, sustained, "TFLOP/s"
-        peak_kind = f"{peak_kind} bf16 sustained (kernel timed inside a long loop)"
+        peak_kind = (f"{peak_kind} bf16 sustained x 2, the nominal E4M3/bf16 dense ratio (kernel timed inside a long loop)"
+                     if args.fp8 else f"{peak_kind} bf16 sustained (kernel timed inside a long loop)")
     else:
         achieved, peak, unit = work / (ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_kind = f"{peak_kind} HBM copy bandwidth"
@@ -425,11 +435,12 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "e4m3" if args.fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "step": "fwd+bwd" if do_bwd else "fwd",
-                   "l2": f"inputs {3 * w.B * w.H * w.N * w.d * 2 / 2**20:.0f} MiB of Q,K,V > L2; no flush",
+                   "l2": f"inputs {3 * w.B * w.H * w.N * w.d * (1 if args.fp8 else 2) / 2**20:.0f} MiB of Q,K,V > L2; "
+                         "no flush",
                    "parallelism": f"heads independent; {world} rank(s) x own batch, no collective",
                    **({"mask": MASKS[args.mask]} if mask is not None else {})},
         "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fwd_tflops, 2),
@@ -442,6 +453,8 @@ def run_ours(args):
         "e2e": e2e,
         **({"note": "with a mask: no e2e (the host pipeline carries no mask), no cpu_baseline, no ncu traffic "
                     "(the profiles cover the unmasked kernels)"} if mask is not None else {}),
+        **({"note": "FP8 forward alone (E4M3 q, k, v^T in HBM, seeded N(0,1) rounded to E4M3): no e2e (the host "
+                    "pipeline runs the bf16 path), no cpu_baseline"} if args.fp8 else {}),
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
@@ -670,8 +683,10 @@ def run_reference_decode(args):
 def main(argv=None):
     args = parse_args(argv)
     from exact_tiled_attention_18_gb300 import workloads
-    if args.mask != "none" and (args.impl == "reference" or args.workload in workloads.DECODE_WORKLOADS):
-        raise SystemExit("--mask applies to our arm on the training workloads only")
+    if (args.mask != "none" or args.fp8) and (args.impl == "reference" or args.workload in workloads.DECODE_WORKLOADS):
+        raise SystemExit("--mask and --fp8 apply to our arm on the training workloads only")
+    if args.fp8 and args.mask != "none":
+        raise SystemExit("--fp8 takes no mask")
     if args.impl == "reference":
         line = run_reference(args)
     elif args.workload in workloads.DECODE_WORKLOADS:
