@@ -2,7 +2,7 @@
 to run out (one tile is left unloaded through the FA_TEST_STALL_UNIT hook),
 and the kernel must return, report FA_ERR_TIMEOUT through fa_sync_status(),
 and leave the context usable for the next call.  Covers the forward, both
-backward kernels and the decode kernel."""
+backward kernels, the decode kernel and the FP8 forward."""
 
 import json
 import os
@@ -36,6 +36,10 @@ if which in ("dq", "dkdv"):
 if which == "decode":
     g = workloads.make_decode_inputs(1, 2, 1, 6000, 64, seed=4)
     dq_, dk_, dv_ = (g[n].cuda() for n in ("q", "k", "v"))
+if which == "fp8":
+    x8 = workloads.make_fp8_inputs(1, 2, 640, 128, seed=5)
+    q8, k8, vt8 = (x8[n].cuda() for n in ("q", "k", "vt"))
+    s8 = float(torch.tensor(128 ** -0.5))
 
 def run():
     if which == "fwd":
@@ -49,6 +53,8 @@ def run():
         os.environ.update(pending)
         fa.backward_stage(1, q, k, v, o, lse, do, *grads, ws, causal=True, scale=scale)
         return grads
+    if which == "fp8":
+        return fa.forward_fp8(q8, k8, vt8, causal=True, scale=s8)
     return fa.forward_decode(dq_, dk_, dv_, causal=True, scale=scale)
 
 out = {{}}
@@ -71,6 +77,13 @@ elif which in ("dq", "dkdv"):
     ref = oracle.backward(x["q"], x["k"], x["v"], x["do"], scale, True)
     idx = 0 if which == "dq" else 1
     out["after_err"] = float(np.abs(res[idx].cpu().double().numpy() - ref[idx]).max())
+elif which == "fp8":
+    # within the bound that rounding P to E4M3 gives (normalised to the 2e-2 check below)
+    vx = {{n: workloads.fp8_values(x8[n]).double().numpy() for n in ("q", "k", "v")}}
+    ref = oracle.forward(vx["q"], vx["k"], vx["v"], s8, True)[0]
+    mass = oracle.forward(vx["q"], vx["k"], np.abs(vx["v"]), s8, True)[0]
+    bound = 2.0 ** -4 * mass + 2.0 ** -10 * np.abs(vx["v"]).sum(axis=2, keepdims=True) + 1e-4
+    out["after_err"] = float((np.abs(res[0].cpu().double().numpy() - ref) / bound).max()) * 2e-2
 else:
     gx = {{n: g[n].float().double().numpy() for n in g}}
     ref = oracle.forward(gx["q"], gx["k"], gx["v"], scale, True)[0]
@@ -79,7 +92,7 @@ print("RESULT " + json.dumps(out))
 """
 
 
-@pytest.mark.parametrize("which", ["fwd", "dq", "dkdv", "decode"])
+@pytest.mark.parametrize("which", ["fwd", "dq", "dkdv", "decode", "fp8"])
 def test_stalled_wait_reports_timeout_and_recovers(which):
     env = dict(os.environ, FA_WAIT_LIMIT_MS="300")
     env.pop("FA_TEST_STALL_UNIT", None)
