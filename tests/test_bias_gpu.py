@@ -210,7 +210,8 @@ def test_backward_dominant_keys_within_rounding_bound():
     unmasked case).  The tensor-core product takes P in bf16 (unit roundoff
     2^-8), which bounds the error of dV_jc by 2^-8 sum_i P_ij |dO_ic|; the
     oracle gives that sum exactly as its dV for |dO|.  dQ and dK keep the
-    plain tolerance."""
+    plain tolerance.  ("FlashAttention Interview Questions", section "Why can
+    recomputation help training?": a tolerance fitted to each configuration.)"""
     B, H, Nq, Nk, d = 2, 3, 400, 400, 128
     g = workloads.make_decode_inputs(B, H, Nq, Nk, d, seed=43)
     do = workloads.randn_bf16((B, H, Nq, d), 47)

@@ -2,7 +2,9 @@
 values.  Parity: LSE to the stated 1e-3; O within the bound that rounding P to
 E4M3 gives, |dO_i| <= 2^-4 sum_j P_ij |v_j| + 2^-10 e^(m_i - LSE_i) sum_j |v_j|
 (relative half-spacing of three mantissa bits; half the subnormal spacing),
-element for element, plus 1e-4 for the fp32 arithmetic."""
+element for element, plus 1e-4 for the fp32 arithmetic.  A tolerance of its
+own for this dtype, as "FlashAttention Interview Questions", section "Why
+can recomputation help training?", asks for each configuration."""
 
 import numpy as np
 import pytest
