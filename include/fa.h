@@ -256,8 +256,11 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
                     const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                     fa_stream_t stream);
 
-/* Gradients of fa_fwd_bias: fa_bwd_ex with the same additive mask (bias and
- * its strides exactly as passed to the forward call that made o and lse).
+/* Gradients of fa_fwd_bias ("FlashAttention Interview Questions", sections
+ * "What is FlashAttention exact about?" for the mask and "Why can
+ * recomputation help training?" for the backward from the saved LSE):
+ * fa_bwd_ex with the same additive mask (bias and its strides exactly as
+ * passed to the forward call that made o and lse).
  * The mask enters only the recomputed probabilities,
  * P_ij = exp(scale * q_i.k_j + bias_ij - LSE_i); it is a constant of the
  * differentiation, so no gradient of the mask is formed.  Rows whose keys
