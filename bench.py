@@ -77,6 +77,8 @@ def parse_args(argv=None):
     p.add_argument("--fwd-only", action="store_true", help="time the forward pass alone")
     p.add_argument("--fp8", action="store_true",
                    help="the forward alone through fa_fwd_fp8 on E4M3 inputs of the workload's shape (d = 128)")
+    p.add_argument("--graph", action="store_true",
+                   help="forward-only steps: capture one step in a CUDA graph and time its replays (launch-bound sizes)")
     p.add_argument("--mask", choices=list(MASKS), default="none",
                    help="general additive mask (fa_fwd_bias / fa_bwd_bias) on the training workloads")
     p.add_argument("--e2e-steps", type=int, default=10)
@@ -326,6 +328,21 @@ def run_ours(args):
     for _ in range(args.warmup):
         step(False)
     fa.sync_status(device)
+    graph = None
+    if args.graph:
+        # one step captured once (the same launches with the same arguments),
+        # replayed without host work between the kernels
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step(False)
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(False)
+        graph.replay()
+        torch.cuda.synchronize(device)
+        fa.sync_status(device)
 
     sampler = ClockSampler(local) if rank == 0 else None
     barrier(dist, device)
@@ -335,7 +352,10 @@ def run_ours(args):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for _ in range(args.steps):
-        step(True)
+        if graph is not None:
+            graph.replay()
+        else:
+            step(True)
     t_end.record(stream)
     torch.cuda.synchronize(device)
     clocks = sampler.stop() if sampler else None
@@ -343,8 +363,10 @@ def run_ours(args):
     fa.sync_status(device)
 
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, device)
-    # per-kernel average duration over the timed steps
-    kern_ms = [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev) for i in range(nev - 1)]
+    # per-kernel average duration over the timed steps (a replayed graph step
+    # is the forward kernel alone)
+    kern_ms = ([total_ms / args.steps] if graph is not None else
+               [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in ev) for i in range(nev - 1)])
     fwd_ms = kern_ms[0]
     bwd_ms = sum(kern_ms[1:]) if do_bwd else 0.0
     ms_per_step = total_ms / args.steps
@@ -442,7 +464,8 @@ def run_ours(args):
                    "l2": f"inputs {3 * w.B * w.H * w.N * w.d * (1 if args.fp8 else 2) / 2**20:.0f} MiB of Q,K,V > L2; "
                          "no flush",
                    "parallelism": f"heads independent; {world} rank(s) x own batch, no collective",
-                   **({"mask": MASKS[args.mask]} if mask is not None else {})},
+                   **({"mask": MASKS[args.mask]} if mask is not None else {}),
+                   **({"launch": "CUDA graph replay of one captured step"} if graph is not None else {})},
         "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fwd_tflops, 2),
                 "frac_of_sustained": round(fwd_tflops / sustained, 4), "frac_of_burst": round(fwd_tflops / burst, 4)},
         "bwd": ({"ms": round(bwd_ms, 4), "tflops": round(bwd_tflops, 2),
@@ -687,6 +710,11 @@ def main(argv=None):
         raise SystemExit("--mask and --fp8 apply to our arm on the training workloads only")
     if args.fp8 and args.mask != "none":
         raise SystemExit("--fp8 takes no mask")
+    if args.graph:
+        from exact_tiled_attention_18_gb300.workloads import WORKLOADS
+        w = WORKLOADS.get(args.workload)
+        if args.impl == "reference" or w is None or (w.backward and not args.fwd_only and not args.fp8):
+            raise SystemExit("--graph applies to forward-only steps of our arm")
     if args.impl == "reference":
         line = run_reference(args)
     elif args.workload in workloads.DECODE_WORKLOADS:

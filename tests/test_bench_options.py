@@ -11,11 +11,13 @@ import bench
     ["--mask", "shared", "--workload", "decode_b8_h32_nq1_nk32768_d128"],
     ["--fp8", "--workload", "decode_b8_h32_nq1_nk32768_d128"],
     ["--fp8", "--mask", "key_row"],
+    ["--graph"],
+    ["--graph", "--impl", "reference", "--workload", "single_head_n256_d64"],
 ])
 def test_variant_options_refused_where_they_do_not_apply(argv):
     with pytest.raises(SystemExit) as e:
         bench.main(argv)
-    assert "apply" in str(e.value) or "no mask" in str(e.value)
+    assert "appl" in str(e.value) or "no mask" in str(e.value)
 
 
 def test_mask_shapes_and_defaults():
