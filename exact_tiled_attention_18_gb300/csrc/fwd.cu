@@ -208,7 +208,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int qtile = 2 * pair + t;
       const int row = qtile * kTileRows + r;
       const int unit = head * sp.units_per_head + pair;
-      float m_ref = 0.f, l = 0.f;
+      // l: running sum of the weights as computed (fp32), for the LSE.  O is
+      // divided by l + dl, where dl sums, over the key tiles, how much the
+      // bf16 rounding (applied to every weight before the P V product)
+      // changed that tile's largest weight.  The reference maximum lags the
+      // row maximum by up to 2^kTau, so a dominant weight is rarely exactly 1;
+      // without dl its rounding would scale a row dominated by one key by up
+      // to 2^-9 (O error near 1e-2 for |v| ~ 5); with it that row returns
+      // the key's value row, and the other weights' rounding stays relative.
+      float m_ref = 0.f, l = 0.f, dl = 0.f;
       // additive mask: this row's bias (bf16, keys contiguous), none for
       // padding rows (fully masked anyway)
       const uint16_t* brow = nullptr;
@@ -323,7 +331,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float t3[5];
 #pragma unroll
         for (int c = 0; c < 5; ++c) t3[c] = fmax3(t2[3 * c], t2[3 * c + 1], t2[3 * c + 2]);
-        const float mt = fmaxf(fmax3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4])) * (BIAS ? 1.f : scale_log2);
+        const float smax = fmaxf(fmax3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4]));
+        const float mt = smax * (BIAS ? 1.f : scale_log2);
         if (j == 0) {
           // without a bias the first key tile holds a key of every row that
           // has one; with a bias it may hide them all, so the reference stays
@@ -338,6 +347,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const float alpha = (BIAS && m_new == -CUDART_INF_F) ? 1.f : ex2_approx(m_ref - m_new);
             m_ref = m_new;
             l *= alpha;
+            dl *= alpha;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
               uint32_t v[32];
@@ -356,6 +366,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float m_use = (BIAS && m_ref == -CUDART_INF_F) ? 0.f : m_ref;  // every t is -inf then
         const uint64_t c2 = f2_pack(cexp, cexp);
         const uint64_t n2 = f2_pack(-m_use, -m_use);
+        {
+          // this tile's largest weight exactly as computed below (the same
+          // fused multiply-add and exponential), and its change by rounding
+          const float pmax = ex2_approx(fmaf(smax, cexp, -m_use));
+          dl += __uint_as_float(pack_bf16x2(pmax, 0.f) << 16) - pmax;
+        }
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -391,7 +407,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // key have l = 0: both get O = 0, LSE = -inf (selected, so that what a
       // padding row accumulated never reaches the output)
       const bool live = l > 0.f && (!VARLEN || row < u.lq);
-      const float inv = live ? 1.0f / l : 0.f;
+      const float inv = live ? 1.0f / (l + dl) : 0.f;
       const bool valid = row < nq;
       float* orow = static_cast<float*>(o) + (static_cast<size_t>(head) * nq + row) * D;
       uint16_t* orow_h = static_cast<uint16_t*>(o) + (static_cast<size_t>(head) * nq + row) * D;
@@ -607,12 +623,8 @@ template <int D, bool CAUSAL, bool VARLEN, bool BIAS = false>
 cudaError_t launch_fwd_v(const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
   auto kern = fwd_kernel<D, CAUSAL, VARLEN, BIAS>;
-  cudaFuncAttributes fattr;
-  cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
-  if (e != cudaSuccess) return e;
-  // the warpgroup register split assumes this launch allocation
-  if (fattr.numRegs != kFwdLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  static std::atomic<unsigned long long> ready{0};
+  const cudaError_t e = setup_kernel_once(kern, L::kSmemBytes, kFwdLaunchRegs, ready);
   if (e != cudaSuccess) return e;
   kern<<<a.sched.grid, kFwdThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.o_bf16, a.geom,
                                                              a.scale_log2, a.sched, a.status, a.wait_limit_ns,

@@ -45,3 +45,29 @@ def assert_forward_close(o, lse, o_ref, lse_ref, what=""):
     le = lse_rel_err(lse, lse_ref)
     assert le <= LSE_REL, f"{what}: LSE rel {le:.3e}"
     return err.max(), err.mean(), le
+
+
+# Row term D_i = sum_j P_ij dP_ij left in the backward workspace.  The kernels
+# form it in fp32 from fp32 probabilities and fp32 dot products, so its error
+# is a small multiple of fp32 rounding of the terms it sums, not of the bf16
+# operands: bounded here by ROW_TERM_REL times D_abs_i = sum_j P_ij sum_c
+# |dO_ic| |v_jc| (the oracle's row term for |dO| and |V|, an upper bound on
+# sum_j P_ij |dP_ij|), plus ROW_TERM_ABS.  At d = 128 with N(0,1) data D_abs
+# is about 80, so the bound is near 1e-3 absolute: far below a row term taken
+# from a wrong or stale row (order 1) or left uncorrected as rowsum(dO o O)
+# of the bf16-rounded forward output (order 1e-2).
+ROW_TERM_REL = 1e-5
+ROW_TERM_ABS = 1e-6
+
+
+def assert_row_term_close(got, ref, ref_abs, what=""):
+    """Element-wise check of the workspace D against the oracle; returns the
+    largest |error| / D_abs seen."""
+    got = np.asarray(got, dtype=np.float64).reshape(np.shape(ref))
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite D"
+    bound = ROW_TERM_REL * ref_abs + ROW_TERM_ABS
+    bad = err > bound
+    assert not bad.any(), (f"{what}: D error {err[bad].max():.3e} above its bound at {int(bad.sum())} rows "
+                           f"(largest error / D_abs {float((err / np.maximum(ref_abs, 1e-30)).max()):.2e})")
+    return float((err / np.maximum(ref_abs, 1e-30)).max())

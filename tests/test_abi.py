@@ -214,3 +214,24 @@ def test_scheduler_rejects_bad_arguments(fa):
         fa.fa_sched_enumerate(0, 128, 64, 0, 1)
     with pytest.raises(ValueError):
         fa.fa_sched_enumerate(1, 128, 80, 0, 1)
+
+
+def test_noalloc_limit_matches_the_header(fa):
+    """The binding's copy of FA_NOALLOC_MAX_ROWS is the header's value."""
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+FA_NOALLOC_MAX_ROWS\s+\(?\s*1\s*<<\s*(\d+)\s*\)?", text)
+    assert m, "FA_NOALLOC_MAX_ROWS not found in include/fa.h"
+    assert fa.binding.FA_NOALLOC_MAX_ROWS == 1 << int(m.group(1))
+
+
+def test_noalloc_rejects_oversize_before_any_other_check(fa):
+    """Above the scratch bound the call fails with FA_ERR_INVALID_ARG even
+    with arguments that would otherwise fail later (a misaligned pointer)."""
+    rows = fa.binding.FA_NOALLOC_MAX_ROWS
+    st = fa.fa_bwd_noalloc(FAKE + 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, rows + 1, 64, 0.125, 0, 0)
+    assert st == 1, fa.fa_status_string(st)
+
+
+def test_stall_hook_argument_check(fa):
+    assert fa.fa_test_set_stall(-2) == 1
+    assert fa.fa_test_set_stall(-1) == 0

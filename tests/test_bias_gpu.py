@@ -8,7 +8,7 @@ import torch
 import exact_tiled_attention_18_gb300 as fa
 import oracle
 from exact_tiled_attention_18_gb300 import workloads
-from tests.helpers import GRAD_MAX_ABS, LSE_REL, O_MAX_ABS, O_MEAN_ABS, scale_for, to64
+from tests.helpers import GRAD_MAX_ABS, LSE_REL, O_MAX_ABS, O_MEAN_ABS, assert_row_term_close, scale_for, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -138,20 +138,32 @@ def _check_grads(got, ref, what):
         assert err <= GRAD_MAX_ABS, (what, name, err)
 
 
-def _grads(q, k, v, do, bias, scale, causal, lq=None, lk=None, o_dtype=None):
+def _grads(q, k, v, do, bias, scale, causal, lq=None, lk=None, o_dtype=None, with_row_term=False):
     qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
     o, lse = fa.forward_bias(qc, kc, vc, bias, lq, lk, causal=causal, scale=scale, o_dtype=o_dtype)
-    g = fa.backward_bias(qc, kc, vc, o, lse, doc, bias, lq, lk, causal=causal, scale=scale)
+    ws = torch.empty(q.shape[0] * q.shape[1] * q.shape[2], dtype=torch.float32, device="cuda")
+    g = fa.backward_bias(qc, kc, vc, o, lse, doc, bias, lq, lk, causal=causal, scale=scale, workspace=ws)
     fa.sync_status()
-    return tuple(t.cpu() for t in g)
+    out = tuple(t.cpu() for t in g)
+    return out + (ws.cpu(),) if with_row_term else out
 
 
-def _ref_grads(q, k, v, do, bias, scale, causal, sq=None, sk=None):
+def _ref_grads(q, k, v, do, bias, scale, causal, sq=None, sk=None, with_row_term=False):
     B, H, Nq, Nk = q.shape[0], q.shape[1], q.shape[2], k.shape[2]
     bb = bias.expand(B, H, Nq, Nk).float().cpu().double().numpy()
     if sq is None:
-        return oracle.backward(to64(q), to64(k), to64(v), to64(do), scale, causal, bb)[:3]
-    return oracle.backward_varlen(to64(q), to64(k), to64(v), to64(do), scale, causal, sq, sk, bb)[:3]
+        r = oracle.backward(to64(q), to64(k), to64(v), to64(do), scale, causal, bb)
+    else:
+        r = oracle.backward_varlen(to64(q), to64(k), to64(v), to64(do), scale, causal, sq, sk, bb)
+    return r if with_row_term else r[:3]
+
+
+def _check_row_term(ws, q, k, v, do, bias, scale, causal, rd, what, sq=None, sk=None):
+    """D in the workspace against the oracle, at the fp32 bound of
+    tests/helpers.py (D_abs from the oracle on |V| and |dO|)."""
+    rd_abs = _ref_grads(q, k, v.abs(), do.abs(), bias, scale, causal, sq, sk, with_row_term=True)[3]
+    rel = assert_row_term_close(ws.numpy(), rd, rd_abs, what)
+    print(f"{what}: D largest error / D_abs {rel:.2e}")
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk,d,causal", [
@@ -168,8 +180,10 @@ def test_backward_random_bias(B, H, Nq, Nk, d, causal):
     do = workloads.randn_bf16((B, H, Nq, d), seed + 3)
     bias = _bias((B, H, Nq, Nk), seed=seed + 4, hide=0.05)
     scale = scale_for(d)
-    got = _grads(g["q"], g["k"], g["v"], do, bias, scale, causal)
-    _check_grads(got, _ref_grads(g["q"], g["k"], g["v"], do, bias, scale, causal), (B, H, Nq, Nk, d, causal))
+    *got, ws = _grads(g["q"], g["k"], g["v"], do, bias, scale, causal, with_row_term=True)
+    ref = _ref_grads(g["q"], g["k"], g["v"], do, bias, scale, causal, with_row_term=True)
+    _check_grads(got, ref[:3], (B, H, Nq, Nk, d, causal))
+    _check_row_term(ws, g["q"], g["k"], g["v"], do, bias, scale, causal, ref[3], (B, H, Nq, Nk, d, causal))
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -185,8 +199,11 @@ def test_backward_hidden_keys_and_rows(d):
     bias = b.cuda()
     scale = scale_for(d)
     for causal in (False, True):
-        got = _grads(g["q"], g["k"], g["v"], do, bias, scale, causal)
-        _check_grads(got, _ref_grads(g["q"], g["k"], g["v"], do, bias, scale, causal), ("hidden", d, causal))
+        *got, ws = _grads(g["q"], g["k"], g["v"], do, bias, scale, causal, with_row_term=True)
+        ref = _ref_grads(g["q"], g["k"], g["v"], do, bias, scale, causal, with_row_term=True)
+        _check_grads(got, ref[:3], ("hidden", d, causal))
+        _check_row_term(ws, g["q"], g["k"], g["v"], do, bias, scale, causal, ref[3], ("hidden", d, causal))
+        assert torch.all(ws.reshape(B, H, N)[0, 0, 5] == 0)
         assert torch.all(got[0][0, 0, 5] == 0)
         assert torch.all(got[1][0, 0, 650:] == 0) and torch.all(got[2][0, 0, 650:] == 0)
 
@@ -222,6 +239,11 @@ def test_backward_dominant_keys_within_rounding_bound():
     _check_grads(got[:2], ref[:2], "dominant keys")
     mass = _ref_grads(g["q"], g["k"], g["v"], do.abs(), bias, scale, True)[2]
     err = np.abs(got[2].double().numpy() - ref[2])
+    # reported against the plain tolerance as well: the kernel feeds P to the
+    # dV product as one bf16 value (a hi + lo pair, one more GEMM per tile,
+    # would bring this under 2e-2)
+    print(f"dominant keys: dV max abs error {err.max():.4f} (plain tolerance {GRAD_MAX_ABS}, "
+          f"{'within' if err.max() <= GRAD_MAX_ABS else 'above'} it), |dV| up to {np.abs(ref[2]).max():.1f}")
     assert np.all(err <= GRAD_MAX_ABS + 2.0 ** -8 * mass), err.max()
 
 
@@ -236,8 +258,11 @@ def test_backward_padded_batch_with_bias():
     lq = torch.tensor(sq, dtype=torch.int32, device="cuda")
     lk = torch.tensor(sk, dtype=torch.int32, device="cuda")
     scale = scale_for(d)
-    got = _grads(g["q"], g["k"], g["v"], do, bias, scale, True, lq, lk, o_dtype=torch.bfloat16)
-    _check_grads(got, _ref_grads(g["q"], g["k"], g["v"], do, bias, scale, True, sq, sk), "padded bias")
+    *got, ws = _grads(g["q"], g["k"], g["v"], do, bias, scale, True, lq, lk, o_dtype=torch.bfloat16,
+                      with_row_term=True)
+    ref = _ref_grads(g["q"], g["k"], g["v"], do, bias, scale, True, sq, sk, with_row_term=True)
+    _check_grads(got, ref[:3], "padded bias")
+    _check_row_term(ws, g["q"], g["k"], g["v"], do, bias, scale, True, ref[3], "padded bias (bf16 O)", sq, sk)
     dq, dk, dv = got
     for b in range(B):
         assert torch.all(dq[b, :, sq[b]:] == 0)

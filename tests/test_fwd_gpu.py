@@ -79,6 +79,32 @@ def test_full_size_sampled_rows(name):
     _sampled(workloads.WORKLOADS[name], 0, 256)
 
 
+@pytest.mark.parametrize("name,heads,last_rows", [
+    ("training_b4_h16_n8192_d128_causal", [(0, 0), (3, 15)], None),
+    ("long_context_b1_h32_n16384_d128_causal", [(0, 17)], None),
+    ("very_long_b1_h8_n65536_d128_causal", [(0, 0)], 4096),
+])
+def test_full_size_whole_heads(name, heads, last_rows):
+    """Full-size forward in the bench's launch configuration, whole heads
+    compared element by element (every tile position and every CTA of the
+    persistent grid that touched them).  The long-context head includes its
+    10x query rows (a late, larger maximum forces the rescale path).  For the
+    N = 65536 workload the last 4096 rows of head 0 are checked against every
+    key they see: with the bottom-right causal alignment of the oracle,
+    queries N-4096..N-1 against all N keys are those rows exactly."""
+    w = workloads.WORKLOADS[name]
+    inp = workloads.workload_inputs(w, 0)
+    o, lse = gpu_forward(inp, w.causal, w.scale)
+    for (b, h) in heads:
+        r0 = 0 if last_rows is None else w.N - last_rows
+        x = {n: to64(inp[n][b:b + 1, h:h + 1]) for n in ("q", "k", "v")}
+        o_ref, lse_ref = oracle.forward(x["q"][:, :, r0:], x["k"], x["v"], w.scale, w.causal)
+        got_o = o.numpy()[b:b + 1, h:h + 1, r0:]
+        got_l = lse.numpy()[b:b + 1, h:h + 1, r0:]
+        mx, mean, le = assert_forward_close(got_o, got_l, o_ref, lse_ref, f"{name} head {(b, h)} rows {r0}..")
+        print(f"{name} head {(b, h)} rows {r0}..{w.N - 1}: O max {mx:.2e} mean {mean:.2e}, LSE rel {le:.2e}")
+
+
 def test_late_large_maximum_rescales():
     """A key in the last tile whose score dwarfs every earlier one moves the
     running maximum late in the sweep (rescaling path)."""
