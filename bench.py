@@ -79,6 +79,9 @@ def parse_args(argv=None):
                    help="the forward alone through fa_fwd_fp8 on E4M3 inputs of the workload's shape (d = 128)")
     p.add_argument("--graph", action="store_true",
                    help="forward-only steps: capture one step in a CUDA graph and time its replays (launch-bound sizes)")
+    p.add_argument("--bwd", choices=["two", "single"], default="two",
+                   help="backward algorithm: two-pass (dQ sweep + dK/dV sweep) or single-pass (row-term pass + "
+                        "one dK/dV/dQ sweep)")
     p.add_argument("--mask", choices=list(MASKS), default="none",
                    help="general additive mask (fa_fwd_bias / fa_bwd_bias) on the training workloads")
     p.add_argument("--e2e-steps", type=int, default=10)
@@ -106,6 +109,8 @@ KERNEL_SOURCES = {
     "dkdv_kernel": ["bwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
     "decode_kernel": ["decode.cu", "geom.cuh", "ptx.cuh", "internal.h"],
     "fwd_fp8_kernel": ["fwd_fp8.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
+    "rowterm_kernel": ["bwd_rowterm.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
+    "dkdv_kernel_dq": ["bwd.cu", "geom.cuh", "ptx.cuh", "fa_sched.h", "internal.h"],
 }
 
 
@@ -317,11 +322,13 @@ def run_ours(args):
             if record:
                 e[2].record(stream)
         elif do_bwd:
-            # fa_bwd's two kernels, one C call each so each can be timed
-            for stage in range(2):
+            # the backward's two kernels, one C call each so each can be timed
+            # (two-pass: stages 0, 1 = fa_bwd; single-pass: stages 2, 3 =
+            # fa_bwd_single_pass)
+            for n, stage in enumerate((0, 1) if args.bwd == "two" else (2, 3)):
                 fa.backward_stage(stage, q, k, v, o, lse, dout, dq, dk, dv, ws, causal=w.causal, scale=w.scale)
                 if record:
-                    e[2 + stage].record(stream)
+                    e[2 + n].record(stream)
         if record:
             ev.append(e)
 
@@ -404,6 +411,30 @@ def run_ours(args):
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "chunks_in_flight": chunks}
 
+    # latency of one forward call through the C ABI itself (no Python
+    # binding): host time to issue a call, and wall time per call when calls
+    # run back to back (whichever of host and device is slower sets it)
+    latency = None
+    if not do_bwd and mask is None and not args.fp8 and graph is None:
+        import ctypes
+        L = fa.binding.lib()
+        cargs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                 ctypes.c_float(w.scale), int(w.causal), int(stream.cuda_stream))
+        n_calls = 500
+        for _ in range(20):
+            L.fa_fwd(*cargs)
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        for _ in range(n_calls):
+            L.fa_fwd(*cargs)
+        t1 = time.perf_counter()
+        torch.cuda.synchronize(device)
+        t2 = time.perf_counter()
+        fa.sync_status(device)
+        latency = {"c_abi_host_us_per_call": round((t1 - t0) * 1e6 / n_calls, 2),
+                   "c_abi_wall_us_per_call": round((t2 - t0) * 1e6 / n_calls, 2),
+                   "python_api_us_per_step": round(total_ms * 1e3 / args.steps, 2), "calls": n_calls}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and mask is None and not args.fp8:
         tf, heads, secs = oracle_sample(w, 0, 10.0)
@@ -414,25 +445,48 @@ def run_ours(args):
     if rank != 0:
         return None
     # an E4M3 contraction takes the bf16 peaks x the nominal dense E4M3/bf16 ratio (4.5 / 2.25)
-    sustained = peaks["bf16_tflops_sustained"] * (2 if args.fp8 else 1)
-    burst = peaks["bf16_tflops"] * (2 if args.fp8 else 1)
+    ratio = 2 if args.fp8 else 1
+    sustained = peaks["bf16_tflops_sustained"] * ratio
+    burst = peaks["bf16_tflops"] * ratio
+    # The measured burst figure is the denominator for a timed region that
+    # runs for less than a second (the clock stays at its maximum); the
+    # sustained one (a seconds-long loop under the power cap) for longer ones.
+    long_region = total_ms >= 1000.0
+    peak_tensor = sustained if long_region else burst
+    peak_tensor_kind = (f"{peak_kind} bf16 {'sustained' if long_region else 'burst'}"
+                        f"{' x 2, the nominal E4M3/bf16 dense ratio' if args.fp8 else ''} "
+                        f"(timed region {total_ms:.0f} ms)")
+    # The theoretical dense peak: SMs x tensor FLOP per clock per SM x clock,
+    # at the maximum SM clock and at the clock sampled during the timed region.
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    flop_clk = 8192 * ratio
+    max_mhz = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
+    med_mhz = (clocks or {}).get("sm_mhz")
+    theo_max = sms * flop_clk * max_mhz * 1e6 / 1e12
+    theo_med = sms * flop_clk * med_mhz * 1e6 / 1e12 if med_mhz else None
     fwd_tflops = w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
     bwd_tflops = w.bwd_flops() / (bwd_ms * 1e-3) / 1e12 if do_bwd else None
     # Algorithmic work per launch of each kernel (one launch covers the whole
-    # batch): forward 2 GEMMs (S, PV); dQ 3 (S, dP, dQ); dK/dV 4 (S, dP, dV,
-    # dK), each 2*N^2*d per head, halved under the causal mask.
+    # batch), in units of one GEMM = 2*N^2*d per head, halved under the
+    # causal mask.  Counted work only: forward 2 (S, PV); the backward's five
+    # (2.5x the forward) are S, dP, dV and dK in the dK/dV kernel and dQ in
+    # the dQ kernel, whose own S and dP are recomputation, not credited.
     gemm = w.fwd_flops() / 2
     kernels = [("fwd_fp8_kernel" if args.fp8 else "fwd_kernel", fwd_ms, "tensor", 2 * gemm)]
+    # The single-pass backward's dK/dV/dQ sweep does all five (its row-term
+    # pass recomputes S and dP for D: no counted work).
     if do_bwd and mask is not None:
-        kernels += [("dq_kernel+dkdv_kernel", kern_ms[1], "tensor", 7 * gemm)]
-    elif do_bwd:
-        kernels += [("dq_kernel", kern_ms[1], "tensor", 3 * gemm),
+        kernels += [("dq_kernel+dkdv_kernel", kern_ms[1], "tensor", 5 * gemm)]
+    elif do_bwd and args.bwd == "two":
+        kernels += [("dq_kernel", kern_ms[1], "tensor", 1 * gemm),
                     ("dkdv_kernel", kern_ms[2], "tensor", 4 * gemm)]
+    elif do_bwd:
+        kernels += [("rowterm_kernel", kern_ms[1], "tensor", 0.0),
+                    ("dkdv_kernel_dq", kern_ms[2], "tensor", 5 * gemm)]
     name, ms, bound, work = max(kernels, key=lambda t: t[1])
     if bound == "tensor":
-        achieved, peak, unit = work / (ms * 1e-3) / 1e12, sustained, "TFLOP/s"
-        peak_kind = (f"{peak_kind} bf16 sustained x 2, the nominal E4M3/bf16 dense ratio (kernel timed inside a long loop)"
-                     if args.fp8 else f"{peak_kind} bf16 sustained (kernel timed inside a long loop)")
+        achieved, peak, unit = work / (ms * 1e-3) / 1e12, peak_tensor, "TFLOP/s"
+        peak_kind = peak_tensor_kind
     else:
         achieved, peak, unit = work / (ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
         peak_kind = f"{peak_kind} HBM copy bandwidth"
@@ -442,6 +496,12 @@ def run_ours(args):
                 "traffic": ncu_traffic(name, w.name) if mask is None else None}
     if bound == "tensor":
         roofline["frac_of_burst_peak"] = round(achieved / burst, 4)
+        roofline["frac_of_sustained_peak"] = round(achieved / sustained, 4)
+        roofline["peak_theoretical"] = {
+            "formula": f"{sms} SMs x {flop_clk} dense FLOP/clk/SM x SM clock",
+            "at_max_clock": {"mhz": max_mhz, "tflops": round(theo_max, 1), "frac": round(achieved / theo_max, 4)},
+            "at_sampled_clock": ({"mhz": med_mhz, "tflops": round(theo_med, 1), "frac": round(achieved / theo_med, 4)}
+                                 if theo_med else None)}
     per_kernel = {n: {"ms": round(t, 4),
                       ("tflops" if b == "tensor" else "gbs"): round(wk / (t * 1e-3) / (1e12 if b == "tensor" else 1e9), 2),
                       "share": round(t / sum(k[1] for k in kernels), 4)}
@@ -461,19 +521,24 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "step": "fwd+bwd" if do_bwd else "fwd",
+                   **({"backward": "single-pass (row-term pass, then one dK/dV/dQ sweep)" if args.bwd == "single"
+                       else "two-pass (dQ sweep, then dK/dV sweep)"} if do_bwd else {}),
                    "l2": f"inputs {3 * w.B * w.H * w.N * w.d * (1 if args.fp8 else 2) / 2**20:.0f} MiB of Q,K,V > L2; "
                          "no flush",
                    "parallelism": f"heads independent; {world} rank(s) x own batch, no collective",
                    **({"mask": MASKS[args.mask]} if mask is not None else {}),
                    **({"launch": "CUDA graph replay of one captured step"} if graph is not None else {})},
         "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fwd_tflops, 2),
-                "frac_of_sustained": round(fwd_tflops / sustained, 4), "frac_of_burst": round(fwd_tflops / burst, 4)},
+                "frac_of_burst": round(fwd_tflops / burst, 4), "frac_of_sustained": round(fwd_tflops / sustained, 4),
+                "frac_of_theoretical_max_clock": round(fwd_tflops / theo_max, 4)},
         "bwd": ({"ms": round(bwd_ms, 4), "tflops": round(bwd_tflops, 2),
-                 "frac_of_sustained": round(bwd_tflops / sustained, 4)} if do_bwd else None),
+                 "frac_of_burst": round(bwd_tflops / burst, 4), "frac_of_sustained": round(bwd_tflops / sustained, 4),
+                 "frac_of_theoretical_max_clock": round(bwd_tflops / theo_max, 4)} if do_bwd else None),
         "kernels": per_kernel,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        **({"latency": latency} if latency else {}),
         **({"note": "with a mask: no e2e (the host pipeline carries no mask), no cpu_baseline, no ncu traffic "
                     "(the profiles cover the unmasked kernels)"} if mask is not None else {}),
         **({"note": "FP8 forward alone (E4M3 q, k, v^T in HBM, seeded N(0,1) rounded to E4M3): no e2e (the host "

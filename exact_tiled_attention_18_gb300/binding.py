@@ -71,6 +71,9 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd.restype = st
         L.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_bwd_varlen.restype = st
+        L.fa_bwd_single_pass.argtypes = [vp, vp, vp, vp, vp, vp, ll, ll, ll, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
+                                         i, vp]
+        L.fa_bwd_single_pass.restype = st
         L.fa_bwd_stage.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_bwd_stage.restype = st
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
@@ -79,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.fa_sync_status.argtypes = [vp]
         L.fa_sync_status.restype = st
+        L.fa_test_set_stall.argtypes = [i]
+        L.fa_test_set_stall.restype = st
         L.fa_last_failure.argtypes = [ctypes.POINTER(ctypes.c_int)]
         L.fa_last_failure.restype = st
         L.fa_status_string.argtypes = [st]
@@ -164,9 +169,17 @@ def fa_bwd_varlen(q: int, k: int, v: int, o: int, lse: int, do: int, dq: int, dk
                                scale, causal, stream)
 
 
+def fa_bwd_single_pass(q: int, k: int, v: int, lse: int, do: int, bias: int, bias_stride_b: int, bias_stride_h: int,
+                       bias_stride_q: int, dq: int, dk: int, dv: int, workspace: int, seqlens_q: int, seqlens_k: int,
+                       B: int, H: int, Nq: int, Nk: int, d: int, scale: float, causal: int, stream: int) -> int:
+    return lib().fa_bwd_single_pass(q, k, v, lse, do, bias, bias_stride_b, bias_stride_h, bias_stride_q, dq, dk, dv,
+                                    workspace, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream)
+
+
 def fa_bwd_stage(stage: int, q: int, k: int, v: int, o: int, lse: int, dO: int, dq: int, dk: int, dv: int,
                  workspace: int, B: int, H: int, N: int, d: int, scale: float, causal: int, stream: int) -> int:
-    """Raw C call of one backward stage (0 dQ and the row term, 1 dK/dV)."""
+    """Raw C call of one backward stage (two-pass: 0 dQ and the row term,
+    1 dK/dV; single-pass: 2 the row term and dQ = 0, 3 dK/dV/dQ)."""
     return lib().fa_bwd_stage(stage, q, k, v, o, lse, dO, dq, dk, dv, workspace, B, H, N, d, scale, causal, stream)
 
 
@@ -186,6 +199,12 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> int:
 
 def fa_sync_status(stream: int) -> int:
     return lib().fa_sync_status(stream)
+
+
+def fa_test_set_stall(unit: int) -> int:
+    """Testing hook: from the next call on, CTA 0 leaves one tile of its
+    unit-th work unit unloaded (-1: off).  Returns the status."""
+    return lib().fa_test_set_stall(int(unit))
 
 
 def fa_last_failure() -> list:
@@ -456,6 +475,42 @@ def _backward(q, k, v, o, lse, do, bias, seqlens_q, seqlens_k, causal, scale, wo
     return dq, dk, dv
 
 
+def backward_single_pass(q, k, v, lse, do, bias=None, seqlens_q=None, seqlens_k=None, causal: bool = False,
+                         scale: float | None = None, workspace=None, out=None):
+    """dQ, dK, dV through fa_bwd_single_pass: q, do [B,H,Nq,d], lse
+    [B,H,Nq], k and v [B,H,Nk,d] (bf16 CUDA); optional bias and seqlens as
+    backward_bias / backward_varlen (fp32 outputs)."""
+    import torch
+    for t in (q, k, v, do):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v, do must be contiguous 4-D bf16 CUDA tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape or do.shape != q.shape:
+        raise ValueError("k, v must be [B, H, Nk, d] and do [B, H, Nq, d]")
+    for t in (seqlens_q, seqlens_k):
+        if t is not None and (not t.is_cuda or t.dtype != torch.int32 or t.numel() != B or not t.is_contiguous()):
+            raise ValueError("seqlens must be contiguous int32 CUDA tensors of B entries")
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    if out is None:
+        dq = torch.empty((B, H, Nq, d), dtype=torch.float32, device=q.device)
+        dk, dv = (torch.empty((B, H, Nk, d), dtype=torch.float32, device=q.device) for _ in range(2))
+    else:
+        dq, dk, dv = out
+    sb = sh = sq = 0
+    if bias is not None:
+        sb, sh, sq = _bias_strides(bias, B, H, Nq, Nk)
+    _check("fa_bwd_single_pass",
+           fa_bwd_single_pass(q.data_ptr(), k.data_ptr(), v.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                              bias.data_ptr() if bias is not None else 0, sb, sh, sq, dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), workspace.data_ptr() if workspace is not None else 0,
+                              seqlens_q.data_ptr() if seqlens_q is not None else 0,
+                              seqlens_k.data_ptr() if seqlens_k is not None else 0,
+                              B, H, Nq, Nk, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    return dq, dk, dv
+
+
 def backward_stage(stage: int, q, k, v, o, lse, do, dq, dk, dv, workspace, causal: bool = False,
                    scale: float | None = None):
     """One backward stage through fa_bwd_stage on the current stream."""
@@ -465,7 +520,8 @@ def backward_stage(stage: int, q, k, v, o, lse, do, dq, dk, dv, workspace, causa
     if scale is None:
         scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
     _check(f"fa_bwd_stage({stage})",
-           fa_bwd_stage(stage, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+           fa_bwd_stage(stage, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr() if o is not None else 0,
+                        lse.data_ptr(),
                         do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
                         B, H, N, d, scale, int(bool(causal)), _stream_handle(q.device)))
 

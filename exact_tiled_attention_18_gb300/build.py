@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
-SOURCES = ["api.cu", "fwd.cu", "fwd_fp8.cu", "bwd.cu", "decode.cu"]
+SOURCES = ["api.cu", "fwd.cu", "fwd_fp8.cu", "bwd.cu", "bwd_rowterm.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

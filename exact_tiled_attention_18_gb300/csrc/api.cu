@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -62,35 +63,74 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 3-D view [heads][n][d] of a contiguous bf16 tensor; box = 64 columns x 128
-// rows x 1 head with 128-byte swizzle (the layout the MMA descriptors
-// expect).  Rows past n read as zeros.
-bool encode_bf16_map(CUtensorMap* m, const void* base, int heads, int n, int d, int box_rows = fa::kTileRows) {
+// Encoded tensor maps, cached by everything that goes into them (base
+// address, element type, extents, box), so that repeated calls on the same
+// tensors skip the driver's encoder.  A map depends on nothing else: reusing
+// one for a buffer freed and allocated again at the same address with the
+// same shape is still exact.  64 entries, replaced round robin.
+struct MapKey {
+  const void* base;
+  int elem_bytes, heads, rows, inner, box_inner, box_rows;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && elem_bytes == o.elem_bytes && heads == o.heads && rows == o.rows && inner == o.inner &&
+           box_inner == o.box_inner && box_rows == o.box_rows;
+  }
+};
+
+constexpr int kMapCacheSize = 64;
+std::mutex g_map_mu;
+MapKey g_map_keys[kMapCacheSize];
+CUtensorMap g_maps[kMapCacheSize];
+int g_map_count = 0, g_map_next = 0;
+
+// 3-D map over [heads][rows][inner] elements of `elem_bytes` (2: bf16, 1:
+// E4M3 bytes), box = box_inner x box_rows x 1 with the 128-byte swizzle (the
+// layout the MMA descriptors expect).  Rows past `rows` read as zeros.
+bool encode_map(CUtensorMap* m, const MapKey& key) {
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < g_map_count; ++i) {
+      if (g_map_keys[i] == key) {
+        *m = g_maps[i];
+        return true;
+      }
+    }
+  }
   auto fn = tensor_map_encoder();
   if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(heads)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(n) * d * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint64_t eb = static_cast<cuuint64_t>(key.elem_bytes);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(key.inner), static_cast<cuuint64_t>(key.rows),
+                        static_cast<cuuint64_t>(key.heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(key.inner) * eb,
+                           static_cast<cuuint64_t>(key.rows) * key.inner * eb};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(key.box_inner), static_cast<cuuint32_t>(key.box_rows), 1};
   cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  CUresult r = fn(m, key.elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3,
+                  const_cast<void*>(key.base), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  int slot;
+  if (g_map_count < kMapCacheSize) {
+    slot = g_map_count++;
+  } else {
+    slot = g_map_next;
+    g_map_next = (g_map_next + 1) % kMapCacheSize;
+  }
+  g_map_keys[slot] = key;
+  g_maps[slot] = *m;
+  return true;
 }
 
-// 3-D map over one-byte elements [heads][rows][inner], 128 x 128 boxes with
-// the 128-byte swizzle (one 128-byte row of the box per matrix row).
+// bf16 [heads][n][d], boxes of 64 columns x box_rows rows.
+bool encode_bf16_map(CUtensorMap* m, const void* base, int heads, int n, int d, int box_rows = fa::kTileRows) {
+  return encode_map(m, MapKey{base, 2, heads, n, d, 64, box_rows});
+}
+
+// one-byte elements [heads][rows][inner], 128 x 128 boxes (one 128-byte row
+// of the box per matrix row).
 bool encode_u8_map(CUtensorMap* m, const void* base, int heads, int rows, int inner) {
-  auto fn = tensor_map_encoder();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows) * inner};
-  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(fa::kTileRows), 1};
-  cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estride,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_map(m, MapKey{base, 1, heads, rows, inner, 128, fa::kTileRows});
 }
 
 unsigned long long wait_limit_ns() {
@@ -103,15 +143,21 @@ unsigned long long wait_limit_ns() {
   return v;
 }
 
-// Testing only: FA_TEST_STALL_UNIT=n makes CTA 0 of the next launches skip one
-// tile load of the n-th work unit it processes (the decode kernel: CTA n skips
-// its first stage), so that a pipeline wait runs out and the timeout path can
-// be exercised without faulting anything.  Read on every call; unset (the
-// default) means never.
-int test_stall_unit() {
-  const char* s = std::getenv("FA_TEST_STALL_UNIT");
-  return (s && *s) ? std::atoi(s) : -1;
+// Testing only: a unit index n >= 0 makes CTA 0 of the next launches skip one
+// tile load of the n-th work unit it processes (the decode kernel: CTA n
+// skips its first stage), so that a pipeline wait runs out and the timeout
+// path can be exercised without faulting anything.  -1 (the default) means
+// never.  Its first value comes from FA_TEST_STALL_UNIT, read once per
+// process; fa_test_set_stall changes it.
+std::atomic<int>& stall_unit_cell() {
+  static std::atomic<int> cell([]() {
+    const char* s = std::getenv("FA_TEST_STALL_UNIT");
+    return (s && *s) ? std::atoi(s) : -1;
+  }());
+  return cell;
 }
+
+int test_stall_unit() { return stall_unit_cell().load(std::memory_order_relaxed); }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -199,10 +245,16 @@ fa_status fwd_common(const void* q, const void* k, const void* v, void* o, int o
 // Checks the arguments of a backward call (the workspace only for alignment;
 // it may be null) and fills every field of `a` but the row-term buffer.  q, dO, o, lse, dq: [B*H][Nq] rows; k, v, dk, dv:
 // [B*H][Nk] rows.
+// need_o = false (the single-pass backward, which forms D without O): o is
+// ignored and may be null.
 fa_status bwd_prepare(fa::BwdArgs& a, const void* q, const void* k, const void* v, const void* o, int o_dtype,
                       const float* lse, const void* dO, float* dq, float* dk, float* dv, const float* workspace,
                       const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale,
-                      int causal) {
+                      int causal, bool need_o = true) {
+  if (!need_o) {
+    o = q;  // never read
+    o_dtype = FA_DTYPE_F32;
+  }
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (o_dtype != FA_DTYPE_F32 && o_dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   fa_status st = check_sizes(B, H, Nq, d, causal);
@@ -472,12 +524,13 @@ static float* g_noalloc_ptr[kMaxDevices];
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const float* o, const float* lse,
                          const void* dO, float* dq, float* dk, float* dv, int B, int H, int N, int d, float scale,
                          int causal, fa_stream_t stream) {
+  // the scratch bound first, before any descriptor is built
+  if (B < 1 || H < 1 || N < 1 || static_cast<long long>(B) * H * N > FA_NOALLOC_MAX_ROWS) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a;
   fa_status st =
       bwd_prepare(a, q, k, v, o, FA_DTYPE_F32, lse, dO, dq, dk, dv, nullptr, nullptr, nullptr, B, H, N, N, d, scale,
                   causal);
   if (st != FA_OK) return st;
-  if (static_cast<long long>(B) * H * N > FA_NOALLOC_MAX_ROWS) return FA_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
   {
@@ -492,14 +545,43 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const floa
   return fa::launch_bwd(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+fa_status fa_bwd_single_pass(const void* q, const void* k, const void* v, const float* lse, const void* dO,
+                             const void* bias, long long bias_stride_b, long long bias_stride_h,
+                             long long bias_stride_q, float* dq, float* dk, float* dv, float* workspace,
+                             const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d,
+                             float scale, int causal, fa_stream_t stream) {
+  if (bias) {
+    const fa_status bs = check_bias(bias, bias_stride_b, bias_stride_h, bias_stride_q, Nk);
+    if (bs != FA_OK) return bs;
+  }
+  fa::BwdArgs a;
+  fa_status st = bwd_prepare(a, q, k, v, nullptr, FA_DTYPE_F32, lse, dO, dq, dk, dv, workspace, seqlens_q, seqlens_k,
+                             B, H, Nq, Nk, d, scale, causal, false);
+  if (st != FA_OK) return st;
+  if (bias) a.bias = fa::BiasRef{static_cast<const uint16_t*>(bias), bias_stride_b, bias_stride_h, bias_stride_q};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* delta = workspace;
+  if (!delta) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&delta), fa_bwd_workspace_bytes(B, H, Nq), s) != cudaSuccess)
+      return FA_ERR_LAUNCH;
+  }
+  a.delta = delta;
+  cudaError_t e = fa::launch_bwd_single_pass(a, s);
+  if (!workspace) {
+    cudaError_t e2 = cudaFreeAsync(delta, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const float* o, const float* lse,
                        const void* dO, float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d,
                        float scale, int causal, fa_stream_t stream) {
-  if (stage < 0 || stage > 1 || !workspace) return FA_ERR_INVALID_ARG;
+  if (stage < 0 || stage > 3 || !workspace) return FA_ERR_INVALID_ARG;
   fa::BwdArgs a;
   fa_status st =
       bwd_prepare(a, q, k, v, o, FA_DTYPE_F32, lse, dO, dq, dk, dv, workspace, nullptr, nullptr, B, H, N, N, d, scale,
-                  causal);
+                  causal, stage < 2);
   if (st != FA_OK) return st;
   a.delta = workspace;
   return fa::launch_bwd_stage(a, stage, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
@@ -519,6 +601,12 @@ fa_status fa_sync_status(fa_stream_t stream) {
     if (cudaMemcpyToSymbol(g_fa_status, zero, sizeof(zero)) != cudaSuccess) return FA_ERR_DEVICE_FAULT;
     return h[0] == FA_ERR_TIMEOUT ? FA_ERR_TIMEOUT : FA_ERR_DEVICE_FAULT;
   }
+  return FA_OK;
+}
+
+fa_status fa_test_set_stall(int unit) {
+  if (unit < -1) return FA_ERR_INVALID_ARG;
+  stall_unit_cell().store(unit, std::memory_order_relaxed);
   return FA_OK;
 }
 

@@ -59,6 +59,9 @@ enum BwdSite : int {
   SITE_Q_MMA_P = 30,
   SITE_Q_EW_DD = 31,
   SITE_Q_DD_EMPTY = 32,
+  SITE_KV_EW_DQ = 61,     // single pass: dQ share of the previous tile computed
+  SITE_KV_EW_DSW = 62,    // single pass: the dS tile's buffer free to write
+  SITE_KV_MMA_DQE = 63,   // single pass: dQ share read out (its columns free)
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl& w, int site, int unit) {
@@ -151,14 +154,23 @@ __device__ __forceinline__ void load_bias_row(const uint16_t* brow, bool vec, in
 
 // ------------------------------------------------------------------ dK / dV
 
-template <int D>
+// DQ: the single-pass variant, which also forms dQ_i += scale dS_ij k_j for
+// every tile it visits and adds it into the fp32 dQ in global memory.  Its
+// dS (bf16, [128 keys][128 queries], the 128-byte swizzled layout a TMA load
+// of such a tile would give) is written to shared memory for that product:
+// at d = 64 into a buffer of its own; at d = 128, where no 32 KB are left,
+// over the dO tile of the current (Q, dO) stage once dV has read it (the
+// stage is then released after the dQ product instead of after dK).
+template <int D, bool DQ = false>
 struct KvLayout {
   static constexpr int kTileBytes = kTileRows * D * 2;
   static constexpr int kStages = (D == 128) ? 2 : 4;  // (Q, dO) ring
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kTileBytes;
   static constexpr int kQdOff = 2 * kTileBytes;             // stage s: Q at +0, dO at +kTileBytes
-  static constexpr int kLdOff = kQdOff + kStages * 2 * kTileBytes;  // stage s: lse2[128], d[128]
+  static constexpr bool kDsOwn = DQ && D == 64;             // dS tile in a buffer of its own
+  static constexpr int kDsOff = kQdOff + kStages * 2 * kTileBytes;
+  static constexpr int kLdOff = kDsOff + (kDsOwn ? kTileRows * kTileRows * 2 : 0);  // stage s: lse2[128], d[128]
   static constexpr int kBarOff = kLdOff + kStages * 1024;
   static constexpr int KV_FULL = 0;
   static constexpr int KV_EMPTY = 1;
@@ -169,14 +181,21 @@ struct KvLayout {
   static constexpr int S_FULL = LD_EMPTY + kStages;  // S^T computed
   static constexpr int DP_FULL = S_FULL + 1;          // dP^T computed
   static constexpr int P_READY = DP_FULL + 1;    // P^T stored (one arrive per elementwise warp)
-  static constexpr int DS_READY = P_READY + 1;   // dS^T hi/lo stored
+  static constexpr int DS_READY = P_READY + 1;   // dS^T hi/lo stored (and, DQ, the bf16 dS tile)
   static constexpr int ACC_FULL = DS_READY + 1;
-  static constexpr int DRAIN = ACC_FULL + 1;
+  static constexpr int DV_DONE = ACC_FULL + 1;   // DQ: dV of the tile done (its dO tile may be overwritten)
+  static constexpr int DQ_FULL = DV_DONE + 1;    // DQ: dQ share of the tile computed
+  static constexpr int DQ_EMPTY = DQ_FULL + 1;   // DQ: dQ share read out (one arrive per elementwise warp)
+  static constexpr int DS_FREE = DQ_EMPTY + 1;   // DQ, own buffer: the dQ product has read the dS tile
+  static constexpr int DRAIN = DS_FREE + 1;
   static constexpr int kNumBars = DRAIN + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
-  // tensor memory columns
+  // tensor memory columns; the dQ share has columns of its own at d = 64 and
+  // reuses the dP^T columns at d = 128 (after dK has read dS^T from them)
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  static constexpr uint32_t kColDQ = (D == 64) ? 256 + 2 * D : kColDP;
+  static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
 };
 
 // 12 warps: two elementwise warpgroups, then TMA (warp 8), MMA (warp 9), the
@@ -191,15 +210,64 @@ constexpr int kKvOtherRegs = 136;
 static_assert(2 * 128 * kKvEwRegs + 128 * kKvOtherRegs <= kKvThreads * kKvLaunchRegs,
               "register split exceeds the launch allocation");
 
-template <int D, bool CAUSAL, bool BIAS>
+// The single-pass variant's dQ share of one key tile: each elementwise
+// thread reads its query row's NC columns (lane = query row) out of tensor
+// memory, the warp releases the columns, and the thread adds the values into
+// the fp32 dQ row in global memory.  Every key tile adds its share, so the
+// order of the sum (and its last bits) varies from run to run.
+template <int NC>
+__device__ __forceinline__ void dq_share_load(uint32_t taddr, uint32_t (&v)[NC / 32][32]) {
+#pragma unroll
+  for (int c = 0; c < NC / 32; ++c) tmem_ld32(taddr + 32 * c, v[c]);
+  tmem_ld_wait();
+}
+
+template <int NC>
+__device__ __forceinline__ void dq_share_add(float* dst, const uint32_t (&v)[NC / 32][32]) {
+#pragma unroll
+  for (int c = 0; c < NC / 32; ++c) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 32 * c + 4 * e),
+                   "f"(__uint_as_float(v[c][4 * e])), "f"(__uint_as_float(v[c][4 * e + 1])),
+                   "f"(__uint_as_float(v[c][4 * e + 2])), "f"(__uint_as_float(v[c][4 * e + 3]))
+                   : "memory");
+    }
+  }
+}
+
+// Reads the pending dQ share (query tile pend_i of head pend_head) out of
+// tensor memory, releases its columns to the MMA thread and adds it into dQ:
+// warpgroup w takes columns [w d/2, (w+1) d/2) of its query rows.  No-op
+// without a pending share.  Returns false if a wait gave up.
+template <int D>
+__device__ __forceinline__ bool dq_share_flush(uint32_t full_bar, uint32_t empty_bar, uint32_t& dqn,
+                                               int& pend_head, int pend_i, int pend_lq, uint32_t taddr, float* dq,
+                                               int nq, int r, int w, const WaitCtl& wc, int unit) {
+  if (pend_head < 0) return true;
+  const bool ok = wait_bounded(full_bar, dqn & 1, wc, SITE_KV_EW_DQ, unit);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  ++dqn;
+  tc_fence_after();
+  uint32_t v[D / 64][32];
+  dq_share_load<D / 2>(taddr, v);
+  tc_fence_before();
+  mbar_arrive_warp(empty_bar);
+  const int qrow = pend_i * kTileRows + r;
+  if (qrow < pend_lq) dq_share_add<D / 2>(dq + (static_cast<size_t>(pend_head) * nq + qrow) * D + w * (D / 2), v);
+  pend_head = -1;
+  return true;
+}
+
+template <int D, bool CAUSAL, bool BIAS, bool DQ>
 __global__ void __launch_bounds__(kKvThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const float* __restrict__ lse, const float* __restrict__ delta, float* __restrict__ dk,
-                float* __restrict__ dv, const SeqGeom geom, const float scale, const float scale_log2,
-                const SchedParams sp, int* status, const unsigned long long limit_ns, const int stall_unit,
-                const BiasRef bias) {
-  using L = KvLayout<D>;
+                float* __restrict__ dv, float* __restrict__ dq, const SeqGeom geom, const float scale,
+                const float scale_log2, const SchedParams sp, int* status, const unsigned long long limit_ns,
+                const int stall_unit, const BiasRef bias) {
+  using L = KvLayout<D, DQ>;
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -224,6 +292,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     mbar_init(bars + 8 * L::P_READY, 8);
     mbar_init(bars + 8 * L::DS_READY, 8);
     mbar_init(bars + 8 * L::ACC_FULL, 1);
+    mbar_init(bars + 8 * L::DV_DONE, 1);
+    mbar_init(bars + 8 * L::DQ_FULL, 1);
+    mbar_init(bars + 8 * L::DQ_EMPTY, 8);
+    mbar_init(bars + 8 * L::DS_FREE, 1);
     mbar_init(bars + 8 * L::DRAIN, 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -244,6 +316,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, status, limit_ns};
   auto BAR = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  // shared-memory address of the bf16 dS tile of ring position qdpos (DQ)
+  auto ds_tile = [&](uint32_t qdpos) -> uint32_t {
+    return L::kDsOwn ? sbase + L::kDsOff : sbase + L::kQdOff + (qdpos % L::kStages) * 2 * L::kTileBytes + L::kTileBytes;
+  };
 
   if (warp < 8) {
     // ------------------------------------------------ P^T and dS^T (thread = key row)
@@ -253,6 +329,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) << 5) << 16;
     const float* ld_base = reinterpret_cast<const float*>(smem + L::kLdOff);
     uint32_t ldn = 0, sn = 0, an = 0;
+    // DQ: dQ shares read out, dS tiles written; the tile whose dQ share is
+    // still to be read (head, query tile; -1: none)
+    uint32_t dqn = 0, dsn = 0;
+    int pend_head = -1, pend_i = 0, pend_lq = 0;
+    const uint32_t dq_cols = tmem + lane_off + L::kColDQ + w * (D / 2);
     SchedIter it = sched_begin(sp);
     int head, j;
     bool ok = true;
@@ -317,19 +398,54 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             pk[c / 2 + 1] = pack_bf16x2(p[2], p[3]);
           }
         };
-        // Phase 2: dS^T = P^T o (dP^T - D), split into hk (hi) and lk (lo)
-        auto dchunk = [&](const uint32_t (&pr)[32], const uint32_t (&dr)[32], int col0, uint32_t (&hk)[16],
+        // Phase 2: dS^T = P^T o (dP^T - D), split into hk (hi) and lk (lo);
+        // DQ: also scale * dS^T rounded to bf16 into the shared dS tile, this
+        // thread's key row, queries [col0, col0 + 32) (four 16-byte chunks of
+        // the 128-byte row of block w, swizzled by the row)
+        const uint64_t sc2 = f2_pack(scale, scale);
+        const bool key_live = j * kTileRows + r < hl.lk;
+        auto dchunk = [&](const uint32_t (&pr)[32], uint32_t (&dr)[32], int col0, uint32_t (&hk)[16],
                           uint32_t (&lk)[16]) {
 #pragma unroll
           for (int c = 0; c < 32; c += 4) {
             const float4 d4 = *reinterpret_cast<const float4*>(dds + col0 + c);
-            float ds[4];
-            f2_unpack(fmul2(f2_from(pr[c], pr[c + 1]), fsub2(f2_from(dr[c], dr[c + 1]), f2_pack(d4.x, d4.y))), ds[0],
-                      ds[1]);
-            f2_unpack(fmul2(f2_from(pr[c + 2], pr[c + 3]), fsub2(f2_from(dr[c + 2], dr[c + 3]), f2_pack(d4.z, d4.w))),
-                      ds[2], ds[3]);
-            split_bf16x2(ds[0], ds[1], hk[c / 2], lk[c / 2]);
-            split_bf16x2(ds[2], ds[3], hk[c / 2 + 1], lk[c / 2 + 1]);
+            if constexpr (!DQ) {
+              float ds[4];
+              f2_unpack(fmul2(f2_from(pr[c], pr[c + 1]), fsub2(f2_from(dr[c], dr[c + 1]), f2_pack(d4.x, d4.y))),
+                        ds[0], ds[1]);
+              f2_unpack(
+                  fmul2(f2_from(pr[c + 2], pr[c + 3]), fsub2(f2_from(dr[c + 2], dr[c + 3]), f2_pack(d4.z, d4.w))),
+                  ds[2], ds[3]);
+              split_bf16x2(ds[0], ds[1], hk[c / 2], lk[c / 2]);
+              split_bf16x2(ds[2], ds[3], hk[c / 2 + 1], lk[c / 2 + 1]);
+            } else {
+              uint64_t ds01 =
+                  fmul2(f2_from(pr[c], pr[c + 1]), fsub2(f2_from(dr[c], dr[c + 1]), f2_pack(d4.x, d4.y)));
+              uint64_t ds23 =
+                  fmul2(f2_from(pr[c + 2], pr[c + 3]), fsub2(f2_from(dr[c + 2], dr[c + 3]), f2_pack(d4.z, d4.w)));
+              float ds[4];
+              f2_unpack(ds01, ds[0], ds[1]);
+              f2_unpack(ds23, ds[2], ds[3]);
+              split_bf16x2(ds[0], ds[1], hk[c / 2], lk[c / 2]);
+              split_bf16x2(ds[2], ds[3], hk[c / 2 + 1], lk[c / 2 + 1]);
+              float q0, q1, q2, q3;
+              f2_unpack(fmul2(ds01, sc2), q0, q1);
+              f2_unpack(fmul2(ds23, sc2), q2, q3);
+              // the dP^T values just consumed make room for the packed pairs;
+              // a key row past the sequence's valid length (not masked
+              // without the causal rule) gives no dQ share
+              dr[c] = key_live ? pack_bf16x2(q0, q1) : 0u;
+              dr[c + 1] = key_live ? pack_bf16x2(q2, q3) : 0u;
+            }
+          }
+          if constexpr (DQ) {
+            const uint32_t row_base = ds_tile(ldn) + w * 16384 + r * 128;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t chunk = static_cast<uint32_t>(((col0 & 63) >> 3) + k);
+              st_shared_v4(row_base + ((chunk ^ (r & 7)) << 4), dr[8 * k], dr[8 * k + 1], dr[8 * k + 4],
+                           dr[8 * k + 5]);
+            }
           }
         };
         // Column slice of this warpgroup: S^T [64w, 64w+64), dP^T likewise.
@@ -356,12 +472,28 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive_warp(BAR(L::P_READY));
+          if constexpr (DQ) {
+            // the previous tile's dQ share (computed while this tile's P ran)
+            ok = dq_share_flush<D>(BAR(L::DQ_FULL), BAR(L::DQ_EMPTY), dqn, pend_head, pend_i, pend_lq, dq_cols, dq,
+                                   geom.nq, r, w, wc, unit);
+            if (!ok) break;
+          }
           ok = warp_wait(BAR(L::DP_FULL), sdp_parity, wc, SITE_KV_EW_DP, unit);
           if (!ok) break;
           tc_fence_after();
           tmem_ld32(tD, d0);
           tmem_ld32(tD + 32, d1);
-          tmem_ld_wait();
+          if constexpr (DQ) {
+            // the dS tile's buffer: free once the previous dQ product read it
+            // (own buffer), or once dV has read the dO tile it overwrites
+            ok = L::kDsOwn ? warp_wait(BAR(L::DS_FREE), (dsn & 1) ^ 1, wc, SITE_KV_EW_DSW, unit)
+                           : warp_wait(BAR(L::DV_DONE), dsn & 1, wc, SITE_KV_EW_DSW, unit);
+            ++dsn;
+            tmem_ld_wait();
+            if (!ok) break;
+          } else {
+            tmem_ld_wait();
+          }
           dchunk(s0, d0, 64 * w, hk, lk);
           tmem_st16(tD, hk);
           tmem_st16(tD + 32, lk);
@@ -371,14 +503,25 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
         tmem_st_wait();
         tc_fence_before();
+        if constexpr (DQ) fence_proxy_async_smem();  // the dS tile, for the tensor core
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(BAR(L::DS_READY));
           mbar_arrive(BAR(L::LD_EMPTY + ls));
         }
         ++ldn;
+        if constexpr (DQ) {
+          pend_head = head;
+          pend_i = i;
+          pend_lq = hl.lq;
+        }
       }
       if (!ok) break;
+      if constexpr (DQ) {
+        ok = dq_share_flush<D>(BAR(L::DQ_FULL), BAR(L::DQ_EMPTY), dqn, pend_head, pend_i, pend_lq, dq_cols, dq,
+                               geom.nq, r, w, wc, unit);
+        if (!ok) break;
+      }
       // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK; key
       // rows past the valid length (and tiles no query sees) get zeros
       const int row = j * kTileRows + r;
@@ -496,6 +639,21 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const uint64_t qd_mn0 = sdesc_sw128(sbase + L::kQdOff, kTileRows * 128, 1024);
       auto q_k = [&](uint32_t pos) { return qd_k0 + static_cast<uint64_t>(pos % S) * (2 * kTileUnits); };
       auto q_mn = [&](uint32_t pos) { return qd_mn0 + static_cast<uint64_t>(pos % S) * (2 * kTileUnits); };
+      // DQ: dQ_i += (scale dS) K, M = 128 queries, N = d, K = 128 keys; the
+      // dS tile and K both MN-major (rows of 64 queries / d columns per key)
+      constexpr uint32_t id_dq = idesc_bf16_f32(128, D, true, true);
+      const uint64_t k_mn = sdesc_sw128(sbase + L::kKOff, kTileRows * 128, 1024);
+      uint32_t dq_issued = 0, dq_freed = 0;
+      // waits until the elementwise warps have read every dQ share issued so
+      // far out of tensor memory (at most one is outstanding)
+      auto wait_dq_free = [&](int unit) -> bool {
+        while (dq_freed < dq_issued) {
+          if (!wait_bounded(BAR(L::DQ_EMPTY), dq_freed & 1, wc, SITE_KV_MMA_DQE, unit)) return false;
+          ++dq_freed;
+        }
+        tc_fence_after();
+        return true;
+      };
       uint32_t kvn = 0, qdpos = 0, pn = 0;
       SchedIter it = sched_begin(sp);
       int head, j;
@@ -530,6 +688,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         if (!ok) break;
         tc_fence_after();
         issue_s(q_k(qdpos));
+        // DQ, d = 128: the dP^T columns hold the last dQ share until it is read
+        if (DQ && L::kColDQ == L::kColDP && !wait_dq_free(unit)) {
+          ok = false;
+          break;
+        }
         issue_dp(q_k(qdpos) + kTileUnits);
         // Per query tile i: dV += P^T dO once P^T is stored; then S^T of tile
         // i+1, which overwrites P^T(i) only after dV(i) has read it (the
@@ -552,6 +715,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
             umma_ts(tmem + L::kColDV, tmem + L::kColS + acol, dmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
                     (!first || ks > 0) ? 1u : 0u);
+          }
+          if constexpr (DQ) {
+            if (!L::kDsOwn) umma_commit(BAR(L::DV_DONE));  // its dO tile becomes the dS tile
           }
           const bool more = i + 1 < i1;
           if (more) {
@@ -576,9 +742,32 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             umma_ts(tmem + L::kColDK, tmem + L::kColDP + acol, qmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
                     1u);
           }
+          if constexpr (DQ) {
+            // this tile's dQ share (at d = 128 over the dP^T columns, which
+            // the dK products above have read: the pipe runs in issue order)
+            if (L::kColDQ != L::kColDP && !wait_dq_free(unit)) {
+              ok = false;
+              break;
+            }
+            const uint64_t ds_mn = sdesc_sw128(ds_tile(qdpos), kTileRows * 128, 1024);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint64_t off = static_cast<uint64_t>((ks * 2048) >> 4);
+              umma_ss(tmem + L::kColDQ, ds_mn + off, k_mn + off, id_dq, ks > 0 ? 1u : 0u);
+            }
+            umma_commit(BAR(L::DQ_FULL));
+            ++dq_issued;
+            if (L::kDsOwn) umma_commit(BAR(L::DS_FREE));
+          }
           umma_commit(BAR(L::QD_EMPTY + s));
           ++qdpos;
-          if (more) issue_dp(q_k(qdpos) + kTileUnits);
+          if (more) {
+            if (DQ && L::kColDQ == L::kColDP && !wait_dq_free(unit)) {
+              ok = false;
+              break;
+            }
+            issue_dp(q_k(qdpos) + kTileUnits);
+          }
         }
         if (!ok) break;
         umma_commit(BAR(L::ACC_FULL));
@@ -667,9 +856,15 @@ struct QLayout {
 };
 
 // 12 warps: two elementwise warpgroups, TMA (warp 8), MMA (warp 9) and the two
-// row-term loaders (warps 10, 11) completing the third warpgroup; same
-// register split as dK/dV.
+// row-term loaders (warps 10, 11) completing the third warpgroup.  Launched
+// at 168 registers a thread: the elementwise warpgroups take 184, the third
+// keeps 136.
 constexpr int kQThreads = 384;
+constexpr int kQLaunchRegs = 168;
+constexpr int kQEwRegs = 184;
+constexpr int kQOtherRegs = 136;
+static_assert(2 * 128 * kQEwRegs + 128 * kQOtherRegs <= kQThreads * kQLaunchRegs,
+              "register split exceeds the launch allocation");
 
 template <int D, bool CAUSAL, bool BIAS>
 __global__ void __launch_bounds__(kQThreads, 1)
@@ -730,7 +925,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
   if (warp < 8) {
     // ------------------------------------------------- dS (thread = query row)
-    regs_increase<kKvEwRegs>();
+    regs_increase<kQEwRegs>();
     // The row term comes in as D'_i = rowsum(dO o O) (computed by the loader
     // warps one unit ahead) with O from the forward pass, whose P was rounded
     // to bf16 for the PV product.  The kernel sees every key of its rows, so
@@ -920,7 +1115,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       }
     }
   } else {
-   regs_decrease<kKvOtherRegs>();
+   regs_decrease<kQOtherRegs>();
    if (warp == 8) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -1170,29 +1365,32 @@ cudaError_t launch_stage_t(const BwdArgs& a, int stage, cudaStream_t stream) {
     // dQ first: it forms D' = rowsum(dO o O) and turns it into the exact row term
     using L = QLayout<D>;
     auto kern = dq_kernel<D, CAUSAL, BIAS>;
-    cudaFuncAttributes fattr;
-    e = cudaFuncGetAttributes(&fattr, kern);
-    if (e != cudaSuccess) return e;
-    if (fattr.numRegs != kKvLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    static std::atomic<unsigned long long> ready{0};
+    e = setup_kernel_once(kern, L::kSmemBytes, kQLaunchRegs, ready);
     if (e != cudaSuccess) return e;
     kern<<<a.grid_q, kQThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.o, a.dout,
                                                          a.o_bf16, a.delta, a.dq, a.geom, a.scale, a.scale_log2,
                                                          a.sched_q, a.status, a.wait_limit_ns, a.stall_unit,
                                                          a.bias);
-  } else {
-    using L = KvLayout<D>;
-    auto kern = dkdv_kernel<D, CAUSAL, BIAS>;
-    cudaFuncAttributes fattr;
-    e = cudaFuncGetAttributes(&fattr, kern);
-    if (e != cudaSuccess) return e;
-    // the warpgroup register split assumes this launch allocation
-    if (fattr.numRegs != kKvLaunchRegs) return cudaErrorInvalidConfiguration;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  } else if (stage == 1) {
+    using L = KvLayout<D, false>;
+    auto kern = dkdv_kernel<D, CAUSAL, BIAS, false>;
+    static std::atomic<unsigned long long> ready{0};
+    e = setup_kernel_once(kern, L::kSmemBytes, kKvLaunchRegs, ready);
     if (e != cudaSuccess) return e;
     kern<<<a.grid_kv, kKvThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dk,
-                                                           a.dv, a.geom, a.scale, a.scale_log2, a.sched_kv, a.status,
-                                                           a.wait_limit_ns, a.stall_unit, a.bias);
+                                                           a.dv, nullptr, a.geom, a.scale, a.scale_log2, a.sched_kv,
+                                                           a.status, a.wait_limit_ns, a.stall_unit, a.bias);
+  } else {
+    // single pass: dK, dV and the dQ shares, after the row-term pass
+    using L = KvLayout<D, true>;
+    auto kern = dkdv_kernel<D, CAUSAL, BIAS, true>;
+    static std::atomic<unsigned long long> ready{0};
+    e = setup_kernel_once(kern, L::kSmemBytes, kKvLaunchRegs, ready);
+    if (e != cudaSuccess) return e;
+    kern<<<a.grid_kv, kKvThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse, a.delta, a.dk,
+                                                           a.dv, a.dq, a.geom, a.scale, a.scale_log2, a.sched_kv,
+                                                           a.status, a.wait_limit_ns, a.stall_unit, a.bias);
   }
   return cudaGetLastError();
 }
@@ -1206,6 +1404,7 @@ cudaError_t launch_stage_c(const BwdArgs& a, int stage, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_bwd_stage(const BwdArgs& a, int stage, cudaStream_t stream) {
+  if (stage == 2) return launch_bwd_rowterm(a, stream);
   if (a.d == 64)
     return a.causal ? launch_stage_c<64, true>(a, stage, stream) : launch_stage_c<64, false>(a, stage, stream);
   return a.causal ? launch_stage_c<128, true>(a, stage, stream) : launch_stage_c<128, false>(a, stage, stream);
@@ -1213,6 +1412,14 @@ cudaError_t launch_bwd_stage(const BwdArgs& a, int stage, cudaStream_t stream) {
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
   for (int stage = 0; stage < 2; ++stage) {
+    const cudaError_t e = launch_bwd_stage(a, stage, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_bwd_single_pass(const BwdArgs& a, cudaStream_t stream) {
+  for (int stage = 2; stage < 4; ++stage) {
     const cudaError_t e = launch_bwd_stage(a, stage, stream);
     if (e != cudaSuccess) return e;
   }

@@ -370,7 +370,8 @@ template <int D, int NQ>
 cudaError_t launch_decode_t(const DecArgs& a, cudaStream_t stream) {
   using L = DecLayout<D, NQ>;
   auto kern = decode_kernel<D, NQ>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  static std::atomic<unsigned long long> ready{0};
+  cudaError_t e = setup_kernel_once(kern, L::kSmemBytes, 0, ready);
   if (e != cudaSuccess) return e;
   const long long grid = static_cast<long long>(a.heads) * a.splits;
   kern<<<static_cast<unsigned>(grid), kDecThreads, L::kSmemBytes, stream>>>(

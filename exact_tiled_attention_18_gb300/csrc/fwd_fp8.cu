@@ -439,12 +439,8 @@ template <bool CAUSAL>
 cudaError_t launch_fp8_t(const FwdArgs& a, cudaStream_t stream) {
   using L = F8Layout;
   auto kern = fwd_fp8_kernel<CAUSAL>;
-  cudaFuncAttributes fattr;
-  cudaError_t e = cudaFuncGetAttributes(&fattr, kern);
-  if (e != cudaSuccess) return e;
-  // the warpgroup register split assumes this launch allocation
-  if (fattr.numRegs != kF8LaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  static std::atomic<unsigned long long> ready{0};
+  const cudaError_t e = setup_kernel_once(kern, L::kSmemBytes, kF8LaunchRegs, ready);
   if (e != cudaSuccess) return e;
   kern<<<a.sched.grid, kF8Threads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, static_cast<float*>(a.o), a.lse,
                                                             a.geom.nq, a.scale_log2, a.sched, a.status,

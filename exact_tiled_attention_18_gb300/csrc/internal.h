@@ -4,11 +4,37 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstdint>
 
 #include "fa_sched.h"
 
 namespace fa {
+
+// One-time setup of a kernel on the current device, before its first launch
+// there: checks the registers per thread it was compiled with (the kernels'
+// warpgroup register splits assume that launch allocation; 0 skips the
+// check) and raises its dynamic shared-memory limit.  `done` holds one bit
+// per device already set up, so later launches skip both runtime calls.
+template <typename Kernel>
+cudaError_t setup_kernel_once(Kernel kern, int smem_bytes, int expect_regs, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ULL << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  if (expect_regs > 0) {
+    cudaFuncAttributes fattr;
+    e = cudaFuncGetAttributes(&fattr, kern);
+    if (e != cudaSuccess) return e;
+    if (fattr.numRegs != expect_regs) return cudaErrorInvalidConfiguration;
+  }
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  done.fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
+}
 
 // Sequence geometry: padded query/key lengths and optional per-sequence valid
 // lengths (device arrays of B ints; null means all rows are valid).
@@ -97,8 +123,12 @@ struct DecArgs {
 
 cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);
 
-// The two stages of launch_bwd, for callers that time or order them
-// separately: 0 = dQ (forms the row term D), 1 = dK/dV.
+// The stages of the two backward algorithms, for callers that time or order
+// them separately.  Two-pass (launch_bwd): 0 = dQ (forms the row term D),
+// 1 = dK/dV.  Single-pass (launch_bwd_single_pass): 2 = the row term D
+// (and dQ set to zero), 3 = dK, dV and dQ accumulated into place.
 cudaError_t launch_bwd_stage(const BwdArgs& a, int stage, cudaStream_t stream);
+cudaError_t launch_bwd_single_pass(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_rowterm(const BwdArgs& a, cudaStream_t stream);
 
 }  // namespace fa

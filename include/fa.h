@@ -41,8 +41,9 @@
  *    kernels is bounded (4 s by default; the FA_WAIT_LIMIT_MS environment
  *    variable, read once per process, changes it), so a failing kernel
  *    returns instead of hanging.  For tests of that path only,
- *    FA_TEST_STALL_UNIT=n (read on every call that launches work) makes the
- *    first CTA leave one tile of its n-th work unit unloaded (fa_fwd_decode:
+ *    fa_test_set_stall(n) (initial value: the FA_TEST_STALL_UNIT environment
+ *    variable, read once per process) makes the first CTA of every later
+ *    launch leave one tile of its n-th work unit unloaded (fa_fwd_decode:
  *    CTA n leaves its first stage unloaded): its waits run out and
  *    fa_sync_status() then reports FA_ERR_TIMEOUT.
  *  - Thread safety: calls may be made from several host threads; calls on
@@ -308,13 +309,45 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const floa
                          int causal, fa_stream_t stream);
 
 /*
- * One stage of fa_bwd, for callers that time or schedule the two kernels
- * separately; running stages 0, 1 in order on one stream is exactly fa_bwd
- * with a caller-owned workspace (here required, never NULL).
+ * Single-pass backward: the same gradients as fa_bwd_bias (bias NULL: as
+ * fa_bwd_varlen), with dQ formed inside the dK/dV sweep instead of by a
+ * second sweep that recomputes S and dP ("FlashAttention Interview Questions
+ * ...", section "Why can recomputation help training?": P is rebuilt from
+ * q, k and the saved lse).  Two kernels run in stream order:
+ *   1. the row term D_i = sum_j P_ij dP_ij, formed from the recomputed fp32
+ *      probabilities (two tensor-core products per tile, S = q k^T and
+ *      dP = dO v^T); it also sets dQ to zero;
+ *   2. one CTA per 128-key tile sweeps the query tiles that see it and forms
+ *      dV += P^T dO, dK += scale dS^T q and each tile's dQ share
+ *      scale dS k, which it adds into dQ in place.
+ * The row term comes from P and dP, not from the forward output, so no O is
+ * taken.  dQ's sum over key tiles runs in an order that varies between runs,
+ * so dQ may differ in its last bits from call to call (dK, dV do not).
+ *   q, k, v, dO, lse, dq, dk, dv, seqlens_q, seqlens_k, B, H, Nq, Nk, d,
+ *   scale, causal : as fa_bwd_varlen.
+ *   bias and its strides : as fa_bwd_bias, or bias = NULL for no mask.
+ *   workspace : fp32, fa_bwd_workspace_bytes(B, H, Nq) bytes, ends holding D;
+ *               or NULL (a stream-ordered allocation, freed on the stream).
+ * Errors as fa_bwd_bias.
+ */
+fa_status fa_bwd_single_pass(const void* q, const void* k, const void* v, const float* lse, const void* dO,
+                             const void* bias, long long bias_stride_b, long long bias_stride_h,
+                             long long bias_stride_q, float* dq, float* dk, float* dv, float* workspace,
+                             const int* seqlens_q, const int* seqlens_k, int B, int H, int Nq, int Nk, int d,
+                             float scale, int causal, fa_stream_t stream);
+
+/*
+ * One stage of a backward pass, for callers that time or schedule the
+ * kernels separately; the workspace is required (never NULL).
  *   stage 0: dQ; also writes the exact row term D_i = sum_j P_ij dP_ij into
  *            the workspace (formed from rowsum(dO o O) inside the kernel).
  *   stage 1: dK and dV (needs stage 0 first).
- * Arguments as fa_bwd; a stage outside 0..1 returns FA_ERR_INVALID_ARG.
+ *            Stages 0, 1 in order on one stream are exactly fa_bwd.
+ *   stage 2: the row term D from the recomputed P and dP, and dQ = 0
+ *            (o is not read and may be NULL).
+ *   stage 3: dK, dV, and dQ accumulated into place (needs stage 2 first).
+ *            Stages 2, 3 in order are fa_bwd_single_pass without a mask.
+ * Arguments as fa_bwd; a stage outside 0..3 returns FA_ERR_INVALID_ARG.
  */
 fa_status fa_bwd_stage(int stage, const void* q, const void* k, const void* v, const float* o, const float* lse,
                        const void* dO, float* dq, float* dk, float* dv, float* workspace, int B, int H, int N, int d,
@@ -340,6 +373,16 @@ fa_status fa_sync_status(fa_stream_t stream);
  * Returns FA_OK, or FA_ERR_INVALID_ARG if out is NULL.
  */
 fa_status fa_last_failure(int out[4]);
+
+/*
+ * Testing hook of the timeout path (see "Errors" above): from the next call
+ * on, the first CTA of each launch leaves one tile of its unit-th work unit
+ * unloaded, so that the waits on it run out and fa_sync_status() reports
+ * FA_ERR_TIMEOUT; unit = -1 switches the hook off (the default unless
+ * FA_TEST_STALL_UNIT was set when the library first launched work).  Nothing
+ * faults or hangs.  Returns FA_OK, or FA_ERR_INVALID_ARG for unit < -1.
+ */
+fa_status fa_test_set_stall(int unit);
 
 /* Static, human-readable name of a status code; never NULL. */
 const char* fa_status_string(fa_status s);

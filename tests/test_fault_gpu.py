@@ -1,8 +1,9 @@
 """Failure detection on the GPU without faulting it: a pipeline wait is made
-to run out (one tile is left unloaded through the FA_TEST_STALL_UNIT hook),
+to run out (one tile is left unloaded through the fa_test_set_stall hook),
 and the kernel must return, report FA_ERR_TIMEOUT through fa_sync_status(),
 and leave the context usable for the next call.  Covers the forward, both
-backward kernels, the decode kernel and the FP8 forward."""
+kernels of each backward algorithm (two-pass and single-pass), the decode
+kernel and the FP8 forward."""
 
 import json
 import os
@@ -28,7 +29,7 @@ scale = float(torch.tensor(64 ** -0.5))
 inp = workloads.make_inputs(1, 2, 600, 64, seed=3, with_grad=True)
 q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
 x = {{n: inp[n].float().double().numpy() for n in inp}}
-if which in ("dq", "dkdv"):
+if which in ("dq", "dkdv", "rowterm", "fused"):
     o, lse = fa.forward(q, k, v, causal=True, scale=scale)
     fa.sync_status()
     grads = [torch.empty(q.shape, dtype=torch.float32, device="cuda") for _ in range(3)]
@@ -50,32 +51,43 @@ def run():
     if which == "dkdv":
         fa.backward_stage(0, q, k, v, o, lse, do, *grads, ws, causal=True, scale=scale)
         fa.sync_status()
-        os.environ.update(pending)
+        fa.fa_test_set_stall(pending)
         fa.backward_stage(1, q, k, v, o, lse, do, *grads, ws, causal=True, scale=scale)
+        return grads
+    if which == "rowterm":
+        fa.backward_stage(2, q, k, v, None, lse, do, *grads, ws, causal=True, scale=scale)
+        if pending == -1:  # the recovery run completes the single pass
+            fa.backward_stage(3, q, k, v, None, lse, do, *grads, ws, causal=True, scale=scale)
+        return grads
+    if which == "fused":
+        fa.backward_stage(2, q, k, v, None, lse, do, *grads, ws, causal=True, scale=scale)
+        fa.sync_status()
+        fa.fa_test_set_stall(pending)
+        fa.backward_stage(3, q, k, v, None, lse, do, *grads, ws, causal=True, scale=scale)
         return grads
     if which == "fp8":
         return fa.forward_fp8(q8, k8, vt8, causal=True, scale=s8)
     return fa.forward_decode(dq_, dk_, dv_, causal=True, scale=scale)
 
 out = {{}}
-pending = {{"FA_TEST_STALL_UNIT": "0"}}
-if which != "dkdv":
-    os.environ.update(pending)
+pending = 0
+if which not in ("dkdv", "fused"):
+    fa.fa_test_set_stall(pending)
 t0 = time.time()
 run()
 out["stalled_status"] = fa.fa_sync_status(stream)
 out["seconds"] = time.time() - t0
 out["failure"] = fa.fa_last_failure()
-os.environ.pop("FA_TEST_STALL_UNIT", None)
-pending = {{}}
+pending = -1
+fa.fa_test_set_stall(pending)
 res = run()
 out["after_status"] = fa.fa_sync_status(stream)
 if which == "fwd":
     ref = oracle.forward(x["q"], x["k"], x["v"], scale, True)[0]
     out["after_err"] = float(np.abs(res[0].cpu().double().numpy() - ref).max())
-elif which in ("dq", "dkdv"):
+elif which in ("dq", "dkdv", "rowterm", "fused"):
     ref = oracle.backward(x["q"], x["k"], x["v"], x["do"], scale, True)
-    idx = 0 if which == "dq" else 1
+    idx = 0 if which in ("dq", "rowterm") else 1
     out["after_err"] = float(np.abs(res[idx].cpu().double().numpy() - ref[idx]).max())
 elif which == "fp8":
     # within the bound that rounding P to E4M3 gives (normalised to the 2e-2 check below)
@@ -92,7 +104,7 @@ print("RESULT " + json.dumps(out))
 """
 
 
-@pytest.mark.parametrize("which", ["fwd", "dq", "dkdv", "decode", "fp8"])
+@pytest.mark.parametrize("which", ["fwd", "dq", "dkdv", "decode", "fp8", "rowterm", "fused"])
 def test_stalled_wait_reports_timeout_and_recovers(which):
     env = dict(os.environ, FA_WAIT_LIMIT_MS="300")
     env.pop("FA_TEST_STALL_UNIT", None)
