@@ -77,6 +77,8 @@ def parse_args(argv=None):
     p.add_argument("--fwd-only", action="store_true", help="time the forward pass alone")
     p.add_argument("--fp8", action="store_true",
                    help="the forward alone through fa_fwd_fp8 on E4M3 inputs of the workload's shape (d = 128)")
+    p.add_argument("--splitkv", action="store_true",
+                   help="forward-only steps through fa_fwd_splitkv (keys split over CTAs; few-query-tile workloads)")
     p.add_argument("--graph", action="store_true",
                    help="forward-only steps: capture one step in a CUDA graph and time its replays (launch-bound sizes)")
     p.add_argument("--bwd", choices=["two", "single"], default="two",
@@ -295,10 +297,21 @@ def run_ours(args):
         ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N) // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
     launches_per_step = 1 + (2 if do_bwd else 0)
+    if args.splitkv:
+        # the split-key forward adds a combine kernel whenever it splits (the
+        # library's rule: one wave over the SMs, <= 16 splits of >= 2 key tiles)
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        nkt, units = -(-N // 128), B * H * -(-N // 256)
+        cap = min(16, max(1, nkt // 2))
+        s_want = 1 if units >= sms else -(-sms // units)
+        chunk = -(-nkt // min(s_want, cap))
+        launches_per_step += 1 if -(-nkt // chunk) > 1 else 0
     mask = make_mask(args.mask, B, H, N, device, rank)
     if args.fp8:
         x8 = workloads.make_fp8_inputs(B, H, N, d, seed=rank)
         q8, k8, vt8 = (x8[n].to(device) for n in ("q", "k", "vt"))
+    ws_split = (torch.empty(fa.fa_fwd_splitkv_workspace_bytes(B, H, N, d) // 4, dtype=torch.float32, device=device)
+                if args.splitkv else None)
 
     ev = []
     # with a mask the backward is one fa_bwd_bias call (its two kernels timed together)
@@ -310,6 +323,8 @@ def run_ours(args):
             e[0].record(stream)
         if args.fp8:
             fa.forward_fp8(q8, k8, vt8, causal=w.causal, scale=w.scale, out=(o, lse))
+        elif args.splitkv:
+            fa.forward_splitkv(q, k, v, causal=w.causal, scale=w.scale, workspace=ws_split, out=(o, lse))
         elif mask is None:
             fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=(o, lse))
         else:
@@ -415,18 +430,24 @@ def run_ours(args):
     # binding): host time to issue a call, and wall time per call when calls
     # run back to back (whichever of host and device is slower sets it)
     latency = None
-    if not do_bwd and mask is None and not args.fp8 and graph is None:
+    if not do_bwd and mask is None and not args.fp8 and graph is None and kern_ms[0] < 0.5:
         import ctypes
         L = fa.binding.lib()
-        cargs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
-                 ctypes.c_float(w.scale), int(w.causal), int(stream.cuda_stream))
+        if args.splitkv:
+            call = L.fa_fwd_splitkv
+            cargs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), ws_split.data_ptr(),
+                     B, H, N, d, ctypes.c_float(w.scale), int(w.causal), int(stream.cuda_stream))
+        else:
+            call = L.fa_fwd
+            cargs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                     ctypes.c_float(w.scale), int(w.causal), int(stream.cuda_stream))
         n_calls = 500
         for _ in range(20):
-            L.fa_fwd(*cargs)
+            call(*cargs)
         torch.cuda.synchronize(device)
         t0 = time.perf_counter()
         for _ in range(n_calls):
-            L.fa_fwd(*cargs)
+            call(*cargs)
         t1 = time.perf_counter()
         torch.cuda.synchronize(device)
         t2 = time.perf_counter()
@@ -472,7 +493,8 @@ def run_ours(args):
     # (2.5x the forward) are S, dP, dV and dK in the dK/dV kernel and dQ in
     # the dQ kernel, whose own S and dP are recomputation, not credited.
     gemm = w.fwd_flops() / 2
-    kernels = [("fwd_fp8_kernel" if args.fp8 else "fwd_kernel", fwd_ms, "tensor", 2 * gemm)]
+    kernels = [("fwd_fp8_kernel" if args.fp8 else ("fwd_kernel (split keys) + combine" if args.splitkv else "fwd_kernel"),
+                fwd_ms, "tensor", 2 * gemm)]
     # The single-pass backward's dK/dV/dQ sweep does all five (its row-term
     # pass recomputes S and dP for D: no counted work).
     if do_bwd and mask is not None:
@@ -527,7 +549,9 @@ def run_ours(args):
                          "no flush",
                    "parallelism": f"heads independent; {world} rank(s) x own batch, no collective",
                    **({"mask": MASKS[args.mask]} if mask is not None else {}),
-                   **({"launch": "CUDA graph replay of one captured step"} if graph is not None else {})},
+                   **({"launch": "CUDA graph replay of one captured step"} if graph is not None else {}),
+                   **({"forward": "fa_fwd_splitkv (keys split over CTAs, merged by log-sum-exp)"} if args.splitkv
+                      else {})},
         "fwd": {"ms": round(fwd_ms, 4), "tflops": round(fwd_tflops, 2),
                 "frac_of_burst": round(fwd_tflops / burst, 4), "frac_of_sustained": round(fwd_tflops / sustained, 4),
                 "frac_of_theoretical_max_clock": round(fwd_tflops / theo_max, 4)},
@@ -775,6 +799,10 @@ def main(argv=None):
         raise SystemExit("--mask and --fp8 apply to our arm on the training workloads only")
     if args.fp8 and args.mask != "none":
         raise SystemExit("--fp8 takes no mask")
+    if args.splitkv:
+        w = workloads.WORKLOADS.get(args.workload)
+        if args.impl == "reference" or w is None or args.fp8 or args.mask != "none" or (w.backward and not args.fwd_only):
+            raise SystemExit("--splitkv applies to forward-only steps of our arm")
     if args.graph:
         from exact_tiled_attention_18_gb300.workloads import WORKLOADS
         w = WORKLOADS.get(args.workload)

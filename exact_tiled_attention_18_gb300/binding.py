@@ -63,6 +63,10 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_bias.restype = st
         L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
         L.fa_fwd_fp8.restype = st
+        L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        L.fa_fwd_splitkv.restype = st
+        L.fa_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i]
+        L.fa_fwd_splitkv_workspace_bytes.restype = ctypes.c_size_t
         L.fa_fwd_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
         L.fa_fwd_decode.restype = st
         L.fa_fwd_decode_workspace_bytes.argtypes = [i, i, i, i, i]
@@ -145,6 +149,15 @@ def fa_bwd_bias(q: int, k: int, v: int, o: int, o_dtype: int, lse: int, do: int,
 def fa_fwd_fp8(q8: int, k8: int, vt8: int, o: int, lse: int, B: int, H: int, N: int, d: int, scale: float,
                causal: int, stream: int) -> int:
     return lib().fa_fwd_fp8(q8, k8, vt8, o, lse, B, H, N, d, scale, causal, stream)
+
+
+def fa_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int, workspace: int, B: int, H: int, N: int, d: int,
+                   scale: float, causal: int, stream: int) -> int:
+    return lib().fa_fwd_splitkv(q, k, v, o, lse, workspace, B, H, N, d, scale, causal, stream)
+
+
+def fa_fwd_splitkv_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return int(lib().fa_fwd_splitkv_workspace_bytes(B, H, N, d))
 
 
 def fa_fwd_decode(q: int, k: int, v: int, o: int, lse: int, seqlens_q: int, seqlens_k: int, workspace: int, B: int,
@@ -259,6 +272,27 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None)
         o, lse = out
     _check("fa_fwd", fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                             B, H, N, d, scale, int(bool(causal)), _stream_handle(q.device)))
+    return o, lse
+
+
+def forward_splitkv(q, k, v, causal: bool = False, scale: float | None = None, workspace=None, out=None):
+    """O, LSE through fa_fwd_splitkv (each query tile's keys split over
+    several CTAs; for batches with few query tiles).  Arguments as forward;
+    ``workspace`` an optional fp32 CUDA tensor of
+    fa_fwd_splitkv_workspace_bytes(B, H, N, d) bytes."""
+    import torch
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(d ** -0.5, dtype=torch.float32))
+    if out is None:
+        o = torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = out
+    _check("fa_fwd_splitkv", fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                            workspace.data_ptr() if workspace is not None else 0, B, H, N, d, scale,
+                                            int(bool(causal)), _stream_handle(q.device)))
     return o, lse
 
 

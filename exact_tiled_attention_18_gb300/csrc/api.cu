@@ -242,6 +242,27 @@ fa_status fwd_common(const void* q, const void* k, const void* v, void* o, int o
   return fa::launch_fwd(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+// Key splits of the split-key forward: at most kMaxKeySplits, at least two
+// key tiles each, and only as many as it takes to fill the SMs once.
+constexpr int kMaxKeySplits = 16;
+
+int key_split_cap(int N) {
+  const int nkt = (N + fa::kTileRows - 1) / fa::kTileRows;
+  const int cap = nkt / 2;
+  return cap < 1 ? 1 : (cap > kMaxKeySplits ? kMaxKeySplits : cap);
+}
+
+void key_splits(int heads, int N, int sms, int& splits, int& chunk) {
+  const int nkt = (N + fa::kTileRows - 1) / fa::kTileRows;
+  const long long units = static_cast<long long>(heads) * ((N + fa::kUnitRows - 1) / fa::kUnitRows);
+  long long s = units >= sms ? 1 : (sms + units - 1) / units;
+  const int cap = key_split_cap(N);
+  if (s > cap) s = cap;
+  if (s < 1) s = 1;
+  chunk = static_cast<int>((nkt + s - 1) / s);
+  splits = (nkt + chunk - 1) / chunk;
+}
+
 // Checks the arguments of a backward call (the workspace only for alignment;
 // it may be null) and fills every field of `a` but the row-term buffer.  q, dO, o, lse, dq: [B*H][Nq] rows; k, v, dk, dv:
 // [B*H][Nk] rows.
@@ -372,6 +393,68 @@ fa_status fa_fwd_bias(const void* q, const void* k, const void* v, void* o, int 
   if (!bias) return FA_ERR_INVALID_ARG;  // fwd_common treats null as no mask
   return fwd_common(q, k, v, o, o_dtype, lse, seqlens_q, seqlens_k, B, H, Nq, Nk, d, scale, causal, stream, bias,
                     bias_stride_b, bias_stride_h, bias_stride_q);
+}
+
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  if (static_cast<long long>(B) * H * N >= (1LL << 31)) return 0;
+  return static_cast<size_t>(B) * H * key_split_cap(N) * N * (d + 1) * sizeof(float);
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, float* o, float* lse, float* workspace, int B,
+                         int H, int N, int d, float scale, int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, N, d, causal);
+  if (st != FA_OK) return st;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      (workspace && !aligned(workspace, 16)))
+    return FA_ERR_MISALIGNED;
+  DeviceInfo di;
+  if (device_info(di) != FA_OK) return FA_ERR_LAUNCH;
+  const int heads = B * H;
+  int splits = 1, chunk = 1;
+  key_splits(heads, N, di.sms, splits, chunk);
+  if (splits == 1) return fwd_common(q, k, v, o, FA_DTYPE_F32, lse, nullptr, nullptr, B, H, N, N, d, scale, causal,
+                                     stream);
+  fa::FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  if (!encode_bf16_map(&a.tm_q, q, heads, N, d) || !encode_bf16_map(&a.tm_k, k, heads, N, d) ||
+      !encode_bf16_map(&a.tm_v, v, heads, N, d))
+    return FA_ERR_LAUNCH;
+  a.o = o;
+  a.lse = lse;
+  a.geom.nq = N;
+  a.geom.nk = N;
+  a.geom.heads_per_batch = H;
+  a.d = d;
+  a.causal = causal;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  // units: (head, query pair, key split), heaviest pairs first under the
+  // causal mask; splits of one pair are consecutive units
+  a.sched = make_sched(heads, N, d, causal, di.sms, 0, fa::kUnitRows, 1, N);
+  a.sched.units_per_head *= splits;
+  const long long units = static_cast<long long>(heads) * a.sched.units_per_head;
+  a.sched.grid = static_cast<int>(units < di.sms ? units : di.sms);
+  a.splits = splits;
+  a.chunk = chunk;
+  a.status = di.status;
+  a.wait_limit_ns = wait_limit_ns();
+  a.stall_unit = test_stall_unit();
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* part = workspace;
+  if (!part) {
+    if (cudaMallocAsync(reinterpret_cast<void**>(&part), fa_fwd_splitkv_workspace_bytes(B, H, N, d), s) !=
+        cudaSuccess)
+      return FA_ERR_LAUNCH;
+  }
+  a.part = part;
+  cudaError_t e = fa::launch_fwd(a, s);
+  if (!workspace) {
+    cudaError_t e2 = cudaFreeAsync(part, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 size_t fa_fwd_decode_workspace_bytes(int B, int H, int Nq, int Nk, int d) {

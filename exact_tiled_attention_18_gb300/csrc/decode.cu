@@ -395,6 +395,16 @@ cudaError_t launch_decode_d(const DecArgs& a, cudaStream_t stream) {
 
 }  // namespace
 
+cudaError_t launch_split_combine(const float* part, float* o, float* lse, int rows, int nq, int splits, int d,
+                                 cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  if (d == 64)
+    decode_combine_kernel<64><<<grid, 256, 0, stream>>>(part, o, lse, rows, nq, splits);
+  else
+    decode_combine_kernel<128><<<grid, 256, 0, stream>>>(part, o, lse, rows, nq, splits);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream) {
   return a.d == 64 ? launch_decode_d<64>(a, stream) : launch_decode_d<128>(a, stream);
 }

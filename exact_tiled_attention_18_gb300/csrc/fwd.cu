@@ -92,28 +92,46 @@ struct FwdLayout {
 // call (Nq = Nk, no per-sequence lengths): offset 0, no padding rows, and tile
 // 2*pair never has more key tiles than 2*pair+1 nor none at all, facts the
 // compiler folds into the loops below.
+//
+// SPLIT (split keys): a scheduler unit is (pair, split); the unit covers key
+// tiles [k0, k0 + chunk) of its pair only, na and nb count the tiles of that
+// range each query tile needs (either may be 0), and the results are partial
+// (combined afterwards by log-sum-exp).
 struct UnitGeom {
   int lq, lk, off, nkt, na, nb;
+  int pair, split, k0;  // SPLIT only: query-tile pair, key split and its first key tile
 };
 
-template <bool VARLEN>
-__device__ __forceinline__ UnitGeom unit_geom(const SeqGeom& g, int head, int pair, bool causal) {
+template <bool VARLEN, bool SPLIT>
+__device__ __forceinline__ UnitGeom unit_geom(const SeqGeom& g, int head, int unit_idx, bool causal, int splits,
+                                              int chunk) {
   UnitGeom u;
+  int pair = unit_idx;
+  if constexpr (SPLIT) {
+    pair = unit_idx / splits;
+    u.pair = pair;
+    u.split = unit_idx - pair * splits;
+  }
   if constexpr (!VARLEN) {
     u.lq = u.lk = g.nq;
     u.off = 0;
     u.nkt = (g.nq + kTileRows - 1) / kTileRows;
     u.na = causal ? min(2 * pair + 1, u.nkt) : u.nkt;
     u.nb = causal ? min(2 * pair + 2, u.nkt) : u.nkt;
-    return u;
+  } else {
+    const HeadLen h = head_len(g, head);
+    u.lq = h.lq;
+    u.lk = h.lk;
+    u.off = h.off;
+    u.nkt = h.nkt;
+    u.na = query_tile_keys(h, 2 * pair, causal);
+    u.nb = query_tile_keys(h, 2 * pair + 1, causal);
   }
-  const HeadLen h = head_len(g, head);
-  u.lq = h.lq;
-  u.lk = h.lk;
-  u.off = h.off;
-  u.nkt = h.nkt;
-  u.na = query_tile_keys(h, 2 * pair, causal);
-  u.nb = query_tile_keys(h, 2 * pair + 1, causal);
+  if constexpr (SPLIT) {
+    u.k0 = u.split * chunk;
+    u.na = max(0, min(u.na - u.k0, chunk));
+    u.nb = max(0, min(u.nb - u.k0, chunk));
+  }
   return u;
 }
 
@@ -134,15 +152,17 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-template <int D, bool CAUSAL, bool VARLEN, bool BIAS>
+template <int D, bool CAUSAL, bool VARLEN, bool BIAS, bool SPLIT>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o, float* __restrict__ lse,
                const int o_bf16, const SeqGeom geom, const float scale_log2, const SchedParams sp,
                int* status, const unsigned long long limit_ns, const int stall_unit,
                const uint16_t* __restrict__ bias, const long long bias_sb, const long long bias_sh,
-               const long long bias_sq) {
+               const long long bias_sq, float* __restrict__ part, const int splits, const int chunk) {
   using L = FwdLayout<D>;
+  // a unit may have no key tile for one of its query tiles, or none at all
+  constexpr bool GEN = VARLEN || SPLIT;
   constexpr int S = L::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -203,9 +223,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     int head, pair;
     bool ok = true;
     while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
-      const UnitGeom u = unit_geom<VARLEN>(geom, head, pair, CAUSAL);
+      const UnitGeom u = unit_geom<VARLEN, SPLIT>(geom, head, pair, CAUSAL, splits, chunk);
       const int nt = t ? u.nb : u.na;
-      const int qtile = 2 * pair + t;
+      const int qtile = 2 * (SPLIT ? u.pair : pair) + t;
       const int row = qtile * kTileRows + r;
       const int unit = head * sp.units_per_head + pair;
       // l: running sum of the weights as computed (fp32), for the LSE.  O is
@@ -229,6 +249,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           bvec = (reinterpret_cast<uintptr_t>(brow) & 15) == 0;
         }
       }
+      if (SPLIT && nt == 0) {
+        // no key tile of this split for this query tile: an empty partial
+        if (row < nq) {
+          const size_t pr = (static_cast<size_t>(head) * splits + u.split) * nq + row;
+          float4* prow = reinterpret_cast<float4*>(part + pr * D);
+#pragma unroll 1
+          for (int c = 0; c < D / 4; ++c) prow[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          part[static_cast<size_t>(sp.heads) * splits * nq * D + pr] = -CUDART_INF_F;
+        }
+        continue;
+      }
       if (VARLEN && nt == 0) {
         // no key for any row of this tile (or all padding): O = 0, LSE = -inf
         if (row < nq) {
@@ -242,10 +273,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         continue;
       }
       for (int j = 0; j < nt; ++j) {
-        // bias of this row's 128 keys of tile j, fetched while S(j) is computed
+        const int jk = SPLIT ? u.k0 + j : j;  // key tile index (j counts the unit's tiles)
+        // bias of this row's 128 keys of tile jk, fetched while S(j) is computed
         uint4 bq[BIAS ? 16 : 1];
         if constexpr (BIAS) {
-          const int col0 = j * kTileRows;
+          const int col0 = jk * kTileRows;
           if (bvec && col0 + kTileRows <= geom.nk) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) bq[i] = __ldg(reinterpret_cast<const uint4*>(brow + col0) + i);
@@ -311,11 +343,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // keys past the valid length, or (causal) past the row's last key; a
         // padding row masks every key, so that it never takes part in the
         // warp's rescale vote and its values cannot change valid rows' rounding
-        const bool diag = CAUSAL && (j * kTileRows + kTileRows - 1 > qtile * kTileRows + u.off);
-        const bool tail = (j == u.nkt - 1) && ((u.lk & (kTileRows - 1)) != 0);
+        const bool diag = CAUSAL && (jk * kTileRows + kTileRows - 1 > qtile * kTileRows + u.off);
+        const bool tail = (jk == u.nkt - 1) && ((u.lk & (kTileRows - 1)) != 0);
         const bool padq = VARLEN && qtile * kTileRows + kTileRows > u.lq;
         if (diag || tail || padq) {
-          const int lim = row < u.lq ? (CAUSAL ? min(row + u.off + 1, u.lk) : u.lk) - j * kTileRows : 0;
+          const int lim = row < u.lq ? (CAUSAL ? min(row + u.off + 1, u.lk) : u.lk) - jk * kTileRows : 0;
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = (c < lim) ? s[c] : -CUDART_INF_F;
         }
@@ -331,8 +363,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float t3[5];
 #pragma unroll
         for (int c = 0; c < 5; ++c) t3[c] = fmax3(t2[3 * c], t2[3 * c + 1], t2[3 * c + 2]);
-        const float smax = fmaxf(fmax3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4]));
-        const float mt = smax * (BIAS ? 1.f : scale_log2);
+        const float mt = fmaxf(fmax3(t3[0], t3[1], t3[2]), fmaxf(t3[3], t3[4])) * (BIAS ? 1.f : scale_log2);
         if (j == 0) {
           // without a bias the first key tile holds a key of every row that
           // has one; with a bias it may hide them all, so the reference stays
@@ -367,9 +398,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint64_t c2 = f2_pack(cexp, cexp);
         const uint64_t n2 = f2_pack(-m_use, -m_use);
         {
-          // this tile's largest weight exactly as computed below (the same
-          // fused multiply-add and exponential), and its change by rounding
-          const float pmax = ex2_approx(fmaf(smax, cexp, -m_use));
+          // this tile's largest weight (as computed below up to the rounding
+          // of the scaled maximum, an ulp of it) and its change by rounding
+          const float pmax = ex2_approx(mt - m_use);
           dl += __uint_as_float(pack_bf16x2(pmax, 0.f) << 16) - pmax;
         }
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
@@ -409,6 +440,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const bool live = l > 0.f && (!VARLEN || row < u.lq);
       const float inv = live ? 1.0f / (l + dl) : 0.f;
       const bool valid = row < nq;
+      if constexpr (SPLIT) {
+        // this split's normalised output and log2-sum-exp, for the combine
+        const size_t pr = (static_cast<size_t>(head) * splits + u.split) * nq + row;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + 32 * c, v);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 w;
+              w.x = __uint_as_float(v[4 * i + 0]) * inv;
+              w.y = __uint_as_float(v[4 * i + 1]) * inv;
+              w.z = __uint_as_float(v[4 * i + 2]) * inv;
+              w.w = __uint_as_float(v[4 * i + 3]) * inv;
+              *reinterpret_cast<float4*>(part + pr * D + 32 * c + 4 * i) = w;
+            }
+          }
+        }
+        if (valid)
+          part[static_cast<size_t>(sp.heads) * splits * nq * D + pr] = live ? m_ref + log2f(l) : -CUDART_INF_F;
+        continue;
+      }
       float* orow = static_cast<float*>(o) + (static_cast<size_t>(head) * nq + row) * D;
       uint16_t* orow_h = static_cast<uint16_t*>(o) + (static_cast<size_t>(head) * nq + row) * D;
 #pragma unroll 1
@@ -458,9 +513,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int head, pair;
       bool ok = true;
       while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
-        const UnitGeom u = unit_geom<VARLEN>(geom, head, pair, CAUSAL);
-        const int nmax = VARLEN ? max(u.na, u.nb) : u.nb;
-        if (VARLEN && nmax == 0) continue;  // nothing to compute for this unit
+        const UnitGeom u = unit_geom<VARLEN, SPLIT>(geom, head, pair, CAUSAL, splits, chunk);
+        const int nmax = GEN ? max(u.na, u.nb) : u.nb;
+        if (GEN && nmax == 0) continue;  // nothing to compute for this unit
         const int unit = head * sp.units_per_head + pair;
         ok = wait_bounded(BAR(L::Q_EMPTY), (qn & 1) ^ 1, wc, SITE_LOAD_Q, unit);
         if (!ok) break;
@@ -471,7 +526,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
           for (int kb = 0; kb < D / 64; ++kb)
             tma_load_3d_hint(sbase + L::kQOff + t * L::kTileBytes + kb * 16384, &tm_q, BAR(L::Q_FULL), kb * 64,
-                             (2 * pair + t) * kTileRows, head, pol_q);
+                             (2 * (SPLIT ? u.pair : pair) + t) * kTileRows, head, pol_q);
         for (int j = 0; j < nmax && ok; ++j) {
 #pragma unroll 1
           for (int w = 0; w < 2; ++w) {
@@ -489,7 +544,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
             for (int kb = 0; kb < D / 64; ++kb)
               tma_load_3d_hint(sbase + L::kRingOff + slot * L::kTileBytes + kb * 16384, tm,
-                               BAR(L::KV_FULL + slot), kb * 64, j * kTileRows, head, pol_kv);
+                               BAR(L::KV_FULL + slot), kb * 64, ((SPLIT ? u.k0 : 0) + j) * kTileRows, head, pol_kv);
             ++kvpos;
           }
         }
@@ -542,9 +597,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int head, pair;
       bool ok = true;
       while (ok && sched_next(it, sp, blockIdx.x, head, pair)) {
-        const UnitGeom u = unit_geom<VARLEN>(geom, head, pair, CAUSAL);
-        const int na = u.na, nb = u.nb, nmax = VARLEN ? max(na, nb) : nb;
-        if (VARLEN && nmax == 0) continue;  // nothing to compute for this unit
+        const UnitGeom u = unit_geom<VARLEN, SPLIT>(geom, head, pair, CAUSAL, splits, chunk);
+        const int na = u.na, nb = u.nb, nmax = GEN ? max(na, nb) : nb;
+        if (GEN && nmax == 0) continue;  // nothing to compute for this unit
         const int unit = head * sp.units_per_head + pair;
         ok = wait_bounded(BAR(L::Q_FULL), qn & 1, wc, SITE_MMA_Q, unit);
         if (!ok) break;
@@ -552,19 +607,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ok = wait_bounded(BAR(L::KV_FULL + kvbase % S), (kvbase / S) & 1, wc, SITE_MMA_KV, unit);
         if (!ok) break;
         tc_fence_after();
-        if (!VARLEN || na > 0) {
+        if (!GEN || na > 0) {
           issue_s(0, slot_addr(kvbase));
           umma_commit(BAR(L::S_FULL + 0));
         }
-        if (!VARLEN || nb > 0) {
+        if (!GEN || nb > 0) {
           issue_s(1, slot_addr(kvbase));
           umma_commit(BAR(L::S_FULL + 1));
         }
         for (int j = 0; j < nmax; ++j) {
           const uint32_t kpos = kvbase + 2 * j, vpos = kpos + 1, knext = kpos + 2;
-          const bool has_a = j < na, next_a = j + 1 < na, has_b = !VARLEN || j < nb, next_b = j + 1 < nb;
+          const bool has_a = j < na, next_a = j + 1 < na, has_b = !GEN || j < nb, next_b = j + 1 < nb;
           umma_commit(BAR(L::KV_EMPTY + kpos % S));  // K_j is free once S(j) of both tiles completes
-          if (!next_b && (!VARLEN || !next_a)) umma_commit(BAR(L::Q_EMPTY));  // the unit's last S has been issued
+          if (!next_b && (!GEN || !next_a)) umma_commit(BAR(L::Q_EMPTY));  // the unit's last S has been issued
           ok = wait_bounded(BAR(L::KV_FULL + vpos % S), (vpos / S) & 1, wc, SITE_MMA_KV, unit);
           if (!ok) break;
           if (has_a) {
@@ -619,22 +674,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool VARLEN, bool BIAS = false>
+template <int D, bool CAUSAL, bool VARLEN, bool BIAS = false, bool SPLIT = false>
 cudaError_t launch_fwd_v(const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto kern = fwd_kernel<D, CAUSAL, VARLEN, BIAS>;
+  auto kern = fwd_kernel<D, CAUSAL, VARLEN, BIAS, SPLIT>;
   static std::atomic<unsigned long long> ready{0};
-  const cudaError_t e = setup_kernel_once(kern, L::kSmemBytes, kFwdLaunchRegs, ready);
+  cudaError_t e = setup_kernel_once(kern, L::kSmemBytes, kFwdLaunchRegs, ready);
   if (e != cudaSuccess) return e;
   kern<<<a.sched.grid, kFwdThreads, L::kSmemBytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.o_bf16, a.geom,
                                                              a.scale_log2, a.sched, a.status, a.wait_limit_ns,
                                                              a.stall_unit, a.bias, a.bias_sb, a.bias_sh,
-                                                             a.bias_sq);
-  return cudaGetLastError();
+                                                             a.bias_sq, a.part, a.splits, a.chunk);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || !SPLIT) return e;
+  // merge the key splits of every query row by their log-sum-exp
+  return launch_split_combine(a.part, static_cast<float*>(a.o), a.lse, a.sched.heads * a.geom.nq, a.geom.nq,
+                              a.splits, D, stream);
 }
 
 template <int D, bool CAUSAL>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  if (a.splits > 1) return launch_fwd_v<D, CAUSAL, false, false, true>(a, stream);
   if (a.bias) return launch_fwd_v<D, CAUSAL, true, true>(a, stream);
   const bool square = !a.geom.seqlens_q && !a.geom.seqlens_k && a.geom.nq == a.geom.nk && !a.o_bf16;
   return square ? launch_fwd_v<D, CAUSAL, false>(a, stream) : launch_fwd_v<D, CAUSAL, true>(a, stream);

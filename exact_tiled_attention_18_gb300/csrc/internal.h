@@ -60,6 +60,13 @@ struct FwdArgs {
   int stall_unit;                // testing: CTA 0 skips one K tile of its n-th unit (-1: never)
   const uint16_t* bias;          // additive mask, bf16, or null; element (b, h, i, j) at
   long long bias_sb, bias_sh, bias_sq;  //   b * bias_sb + h * bias_sh + i * bias_sq + j
+  // key splits (square fp32 forward only): splits > 1 divides every query
+  // pair's key tiles into ranges of `chunk` tiles, one work unit each
+  // (sched.units_per_head = pairs * splits); the partial results go to part,
+  // [heads][splits][Nq][d] outputs then [heads][splits][Nq] log2-sum-exp,
+  // and are merged into o and lse by launch_split_combine.
+  int splits, chunk;
+  float* part;
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
@@ -122,6 +129,11 @@ struct DecArgs {
 };
 
 cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);
+
+// Merges per-split normalised outputs and their log2-sum-exp (layout of
+// DecArgs::part, `rows` = heads * nq rows) into o and lse (natural log).
+cudaError_t launch_split_combine(const float* part, float* o, float* lse, int rows, int nq, int splits, int d,
+                                 cudaStream_t stream);
 
 // The stages of the two backward algorithms, for callers that time or order
 // them separately.  Two-pass (launch_bwd): 0 = dQ (forms the row term D),

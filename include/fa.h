@@ -118,6 +118,29 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, float* o, f
                         const int* seqlens_k, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                         fa_stream_t stream);
 
+/*
+ * Forward pass with each query tile's keys split over several CTAs: the same
+ * result as fa_fwd (to fp32 rounding), for batches with too few query tiles
+ * to fill the GPU (one head of a few thousand tokens has a few dozen).  Each
+ * split runs the online softmax ("FlashAttention Interview Questions ...",
+ * section "How can softmax be computed across tiles?") over its own range of
+ * key tiles and leaves a normalised partial output and its log-sum-exp; a
+ * second kernel merges the partials by that log-sum-exp -- the same
+ * merge-by-rescaling the online softmax applies from tile to tile.  The
+ * library picks the number of splits from the device's SM count (at most
+ * 16, at least two key tiles each); when one split suffices it runs fa_fwd.
+ *   workspace : fp32 scratch of fa_fwd_splitkv_workspace_bytes(B, H, N, d)
+ *               bytes, 16-byte aligned; or NULL (a stream-ordered allocation,
+ *               freed on the same stream).
+ * Other arguments, results and errors as fa_fwd.
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, float* o, float* lse, float* workspace, int B,
+                         int H, int N, int d, float scale, int causal, fa_stream_t stream);
+
+/* Bytes of the fa_fwd_splitkv workspace (an upper bound that does not depend
+ * on the device); 0 on invalid sizes. */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int N, int d);
+
 /* Most query rows per head that fa_fwd_decode accepts. */
 #define FA_DECODE_MAX_Q 8
 

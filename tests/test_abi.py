@@ -235,3 +235,24 @@ def test_noalloc_rejects_oversize_before_any_other_check(fa):
 def test_stall_hook_argument_check(fa):
     assert fa.fa_test_set_stall(-2) == 1
     assert fa.fa_test_set_stall(-1) == 0
+
+
+def test_splitkv_workspace_bytes(fa):
+    """Bound: heads x min(16, max(1, key tiles / 2)) splits x N rows x (d + 1) fp32."""
+    assert fa.fa_fwd_splitkv_workspace_bytes(1, 1, 4096, 64) == 16 * 4096 * 65 * 4
+    assert fa.fa_fwd_splitkv_workspace_bytes(1, 1, 300, 64) == 1 * 300 * 65 * 4
+    assert fa.fa_fwd_splitkv_workspace_bytes(2, 3, 1500, 128) == 6 * 6 * 1500 * 129 * 4  # 12 key tiles
+    assert fa.fa_fwd_splitkv_workspace_bytes(0, 1, 1, 64) == 0
+    assert fa.fa_fwd_splitkv_workspace_bytes(1, 1, 128, 96) == 0
+
+
+@pytest.mark.parametrize("args,expect", [
+    (dict(q=0), 1), (dict(B=0), 1), (dict(causal=3), 1), (dict(d=80), 2), (dict(o=FAKE + 4), 3),
+    (dict(ws=FAKE + 8), 3), (dict(scale=-1.0), 1),
+])
+def test_splitkv_argument_errors(fa, args, expect):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, ws=FAKE, B=1, H=1, N=1000, d=64, scale=0.125, causal=0)
+    a.update(args)
+    st = fa.fa_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["ws"], a["B"], a["H"], a["N"], a["d"],
+                           a["scale"], a["causal"], 0)
+    assert st == expect, fa.fa_status_string(st)
