@@ -316,9 +316,11 @@ def run_ours(args):
     ev = []
     # with a mask the backward is one fa_bwd_bias call (its two kernels timed together)
     nev = (4 if mask is None else 3) if do_bwd else 2
+    # events of every timed step, created before the timed region
+    pool = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
 
     def step(record):
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(nev)] if record else None
+        e = pool[len(ev)] if record else None
         if record:
             e[0].record(stream)
         if args.fp8:
@@ -452,9 +454,23 @@ def run_ours(args):
         torch.cuda.synchronize(device)
         t2 = time.perf_counter()
         fa.sync_status(device)
+        # the same calls through the Python binding (argument checks, stream lookup, ctypes)
+        fwd_py = (lambda: fa.forward_splitkv(q, k, v, causal=w.causal, scale=w.scale, workspace=ws_split,
+                                             out=(o, lse))) if args.splitkv else \
+            (lambda: fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=(o, lse)))
+        torch.cuda.synchronize(device)
+        t3 = time.perf_counter()
+        for _ in range(n_calls):
+            fwd_py()
+        t4 = time.perf_counter()
+        torch.cuda.synchronize(device)
+        t5 = time.perf_counter()
+        fa.sync_status(device)
         latency = {"c_abi_host_us_per_call": round((t1 - t0) * 1e6 / n_calls, 2),
                    "c_abi_wall_us_per_call": round((t2 - t0) * 1e6 / n_calls, 2),
-                   "python_api_us_per_step": round(total_ms * 1e3 / args.steps, 2), "calls": n_calls}
+                   "python_api_host_us_per_call": round((t4 - t3) * 1e6 / n_calls, 2),
+                   "python_api_wall_us_per_call": round((t5 - t3) * 1e6 / n_calls, 2),
+                   "bench_step_us": round(total_ms * 1e3 / args.steps, 2), "calls": n_calls}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and mask is None and not args.fp8:
