@@ -391,7 +391,7 @@ fa_status fa_sync_status(fa_stream_t stream);
 /*
  * Details of the last device-side failure read by fa_sync_status():
  * out[0] status code, out[1] wait site, out[2] block index, out[3] work unit.
- * Wait sites: 1-8 forward, 11-20 dK/dV, 21-32 dQ, 35-36 decode, 41-47 FP8
+ * Wait sites: 1-7 forward, 11-20 dK/dV, 21-32 dQ, 35-36 decode, 41-47 FP8
  * forward, 51-59 the single-pass row-term pass, 61-63 the single-pass dK/dV
  * sweep (each kernel's source names them).
  * Returns FA_OK, or FA_ERR_INVALID_ARG if out is NULL.
