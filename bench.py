@@ -815,6 +815,11 @@ def main(argv=None):
         raise SystemExit("--mask and --fp8 apply to our arm on the training workloads only")
     if args.fp8 and args.mask != "none":
         raise SystemExit("--fp8 takes no mask")
+    if args.bwd == "single":
+        w = workloads.WORKLOADS.get(args.workload)
+        if (args.impl == "reference" or w is None or not w.backward or args.fwd_only or args.fp8
+                or args.mask != "none"):
+            raise SystemExit("--bwd single applies to unmasked forward+backward steps of our arm")
     if args.splitkv:
         w = workloads.WORKLOADS.get(args.workload)
         if args.impl == "reference" or w is None or args.fp8 or args.mask != "none" or (w.backward and not args.fwd_only):

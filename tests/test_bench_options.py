@@ -13,6 +13,13 @@ import bench
     ["--fp8", "--mask", "key_row"],
     ["--graph"],
     ["--graph", "--impl", "reference", "--workload", "single_head_n256_d64"],
+    ["--splitkv"],                                          # a forward+backward workload
+    ["--splitkv", "--impl", "reference", "--workload", "memory_exercise_n4096_d64"],
+    ["--splitkv", "--fp8", "--workload", "memory_exercise_n4096_d64"],
+    ["--bwd", "single", "--impl", "reference"],
+    ["--bwd", "single", "--mask", "per_head"],
+    ["--bwd", "single", "--fwd-only"],
+    ["--bwd", "single", "--workload", "memory_exercise_n4096_d64"],
 ])
 def test_variant_options_refused_where_they_do_not_apply(argv):
     with pytest.raises(SystemExit) as e:
@@ -30,3 +37,10 @@ def test_mask_shapes_and_defaults():
     assert tuple(bench.make_mask("shared", 2, 3, 16, "cpu", 0).shape) == (1, 1, 16, 16)
     assert tuple(bench.make_mask("per_head", 2, 3, 16, "cpu", 0).shape) == (1, 3, 16, 16)
     assert "fwd_fp8_kernel" in bench.KERNEL_SOURCES
+
+
+def test_backward_and_split_options_defaults():
+    args = bench.parse_args([])
+    assert args.bwd == "two" and not args.splitkv
+    for k in ("rowterm_kernel", "dkdv_kernel_dq"):
+        assert k in bench.KERNEL_SOURCES
