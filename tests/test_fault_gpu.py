@@ -3,7 +3,7 @@ to run out (one tile is left unloaded through the fa_test_set_stall hook),
 and the kernel must return, report FA_ERR_TIMEOUT through fa_sync_status(),
 and leave the context usable for the next call.  Covers the forward, both
 kernels of each backward algorithm (two-pass and single-pass), the decode
-kernel and the FP8 forward."""
+kernel, the FP8 forward and the split-key forward."""
 
 import json
 import os
@@ -37,6 +37,9 @@ if which in ("dq", "dkdv", "rowterm", "fused"):
 if which == "decode":
     g = workloads.make_decode_inputs(1, 2, 1, 6000, 64, seed=4)
     dq_, dk_, dv_ = (g[n].cuda() for n in ("q", "k", "v"))
+if which == "splitkv":
+    xs = workloads.make_inputs(1, 1, 2000, 64, seed=6)
+    qs, ks, vs = (xs[n].cuda() for n in ("q", "k", "v"))
 if which == "fp8":
     x8 = workloads.make_fp8_inputs(1, 2, 640, 128, seed=5)
     q8, k8, vt8 = (x8[n].cuda() for n in ("q", "k", "vt"))
@@ -67,6 +70,8 @@ def run():
         return grads
     if which == "fp8":
         return fa.forward_fp8(q8, k8, vt8, causal=True, scale=s8)
+    if which == "splitkv":
+        return fa.forward_splitkv(qs, ks, vs, causal=True, scale=scale)
     return fa.forward_decode(dq_, dk_, dv_, causal=True, scale=scale)
 
 out = {{}}
@@ -89,6 +94,10 @@ elif which in ("dq", "dkdv", "rowterm", "fused"):
     ref = oracle.backward(x["q"], x["k"], x["v"], x["do"], scale, True)
     idx = 0 if which in ("dq", "rowterm") else 1
     out["after_err"] = float(np.abs(res[idx].cpu().double().numpy() - ref[idx]).max())
+elif which == "splitkv":
+    xx = {{n: xs[n].float().double().numpy() for n in xs}}
+    ref = oracle.forward(xx["q"], xx["k"], xx["v"], scale, True)[0]
+    out["after_err"] = float(np.abs(res[0].cpu().double().numpy() - ref).max())
 elif which == "fp8":
     # within the bound that rounding P to E4M3 gives (normalised to the 2e-2 check below)
     vx = {{n: workloads.fp8_values(x8[n]).double().numpy() for n in ("q", "k", "v")}}
@@ -104,7 +113,7 @@ print("RESULT " + json.dumps(out))
 """
 
 
-@pytest.mark.parametrize("which", ["fwd", "dq", "dkdv", "decode", "fp8", "rowterm", "fused"])
+@pytest.mark.parametrize("which", ["fwd", "dq", "dkdv", "decode", "fp8", "rowterm", "fused", "splitkv"])
 def test_stalled_wait_reports_timeout_and_recovers(which):
     env = dict(os.environ, FA_WAIT_LIMIT_MS="300")
     env.pop("FA_TEST_STALL_UNIT", None)

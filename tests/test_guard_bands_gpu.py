@@ -141,3 +141,22 @@ def test_allocation_free_backward():
                            g[0].t.data_ptr(), g[1].t.data_ptr(), g[2].t.data_ptr(), B, H, N, d, scale, 1, stream)
     assert st == 0, fa.fa_status_string(st)
     _check("noalloc", *g)
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_single_pass_backward(d, causal):
+    """The single-pass backward adds every key tile's dQ share into dQ with
+    reductions: none may land outside dQ (padded batch, ragged lengths)."""
+    B, H, Nq, Nk = 3, 2, 300, 260
+    sq, sk = [300, 0, 129], [260, 77, 200]
+    g = workloads.make_decode_inputs(B, H, Nq, Nk, d, seed=461 + d)
+    q, k, v = (g[n].cuda() for n in ("q", "k", "v"))
+    do = workloads.randn_bf16((B, H, Nq, d), 463 + d).cuda()
+    lq = torch.tensor(sq, dtype=torch.int32, device="cuda")
+    lk = torch.tensor(sk, dtype=torch.int32, device="cuda")
+    o, lse = fa.forward_varlen(q, k, v, lq, lk, causal=causal)
+    dq = Banded((B, H, Nq, d), torch.float32)
+    dk, dv = Banded((B, H, Nk, d), torch.float32), Banded((B, H, Nk, d), torch.float32)
+    ws = Banded((B * H * Nq,), torch.float32)
+    fa.backward_single_pass(q, k, v, lse, do, None, lq, lk, causal=causal, workspace=ws.t, out=(dq.t, dk.t, dv.t))
+    _check(("single pass", d, causal), dq, dk, dv, ws)
