@@ -632,17 +632,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       // Descriptors built once; a stage or K step only moves the start-address
       // field (16-byte units), a plain add.  K-major views feed S^T and dP^T,
       // MN-major views (next 64-column block 16 KB away) feed dV and dK.
-      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
-      const uint64_t kdesc = sdesc_sw128(sbase + L::kKOff, 16, 1024);
-      const uint64_t vdesc = sdesc_sw128(sbase + L::kVOff, 16, 1024);
-      const uint64_t qd_k0 = sdesc_sw128(sbase + L::kQdOff, 16, 1024);
-      const uint64_t qd_mn0 = sdesc_sw128(sbase + L::kQdOff, kTileRows * 128, 1024);
-      auto q_k = [&](uint32_t pos) { return qd_k0 + static_cast<uint64_t>(pos % S) * (2 * kTileUnits); };
-      auto q_mn = [&](uint32_t pos) { return qd_mn0 + static_cast<uint64_t>(pos % S) * (2 * kTileUnits); };
+      constexpr uint32_t kTileUnits = L::kTileBytes >> 4;
+      const SDesc kdesc = sdesc_sw128(sbase + L::kKOff, 16, 1024);
+      const SDesc vdesc = sdesc_sw128(sbase + L::kVOff, 16, 1024);
+      const SDesc qd_k0 = sdesc_sw128(sbase + L::kQdOff, 16, 1024);
+      const SDesc qd_mn0 = sdesc_sw128(sbase + L::kQdOff, kTileRows * 128, 1024);
+      auto q_k = [&](uint32_t pos) { return qd_k0 + (pos % S) * (2 * kTileUnits); };
+      auto q_mn = [&](uint32_t pos) { return qd_mn0 + (pos % S) * (2 * kTileUnits); };
       // DQ: dQ_i += (scale dS) K, M = 128 queries, N = d, K = 128 keys; the
       // dS tile and K both MN-major (rows of 64 queries / d columns per key)
       constexpr uint32_t id_dq = idesc_bf16_f32(128, D, true, true);
-      const uint64_t k_mn = sdesc_sw128(sbase + L::kKOff, kTileRows * 128, 1024);
+      const SDesc k_mn = sdesc_sw128(sbase + L::kKOff, kTileRows * 128, 1024);
       uint32_t dq_issued = 0, dq_freed = 0;
       // waits until the elementwise warps have read every dQ share issued so
       // far out of tensor memory (at most one is outstanding)
@@ -668,18 +668,18 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         ++kvn;
         // S^T = K Q^T and dP^T = V dO^T of one query tile: M = 128 keys,
         // N = 128 queries, K = d
-        auto issue_s = [&](uint64_t qd) {
+        auto issue_s = [&](SDesc qd) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
             umma_ss(tmem + L::kColS, kdesc + off, qd + off, id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::S_FULL));
         };
-        auto issue_dp = [&](uint64_t dd) {
+        auto issue_dp = [&](SDesc dd) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
             umma_ss(tmem + L::kColDP, vdesc + off, dd + off, id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::DP_FULL));
@@ -704,8 +704,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         // [64 w, 64 w + 32) and [64 w + 32, 64 w + 64).
         for (int i = i0; i < i1; ++i) {
           const uint32_t s = qdpos % S;
-          const uint64_t qmn = q_mn(qdpos);
-          const uint64_t dmn = qmn + kTileUnits;
+          const SDesc qmn = q_mn(qdpos);
+          const SDesc dmn = qmn + kTileUnits;
           ok = wait_bounded(BAR(L::P_READY), pn & 1, wc, SITE_KV_MMA_PDS, unit);
           if (!ok) break;
           tc_fence_after();
@@ -713,7 +713,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDV, tmem + L::kColS + acol, dmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
+            umma_ts(tmem + L::kColDV, tmem + L::kColS + acol, dmn + static_cast<uint32_t>((ks * 2048) >> 4), id_acc,
                     (!first || ks > 0) ? 1u : 0u);
           }
           if constexpr (DQ) {
@@ -733,13 +733,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDK, tmem + L::kColDP + acol, qmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
+            umma_ts(tmem + L::kColDK, tmem + L::kColDP + acol, qmn + static_cast<uint32_t>((ks * 2048) >> 4), id_acc,
                     (!first || ks > 0) ? 1u : 0u);
           }
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {  // dS^T lo part
             const uint32_t acol = 32 + 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDK, tmem + L::kColDP + acol, qmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
+            umma_ts(tmem + L::kColDK, tmem + L::kColDP + acol, qmn + static_cast<uint32_t>((ks * 2048) >> 4), id_acc,
                     1u);
           }
           if constexpr (DQ) {
@@ -749,10 +749,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               ok = false;
               break;
             }
-            const uint64_t ds_mn = sdesc_sw128(ds_tile(qdpos), kTileRows * 128, 1024);
+            const SDesc ds_mn = sdesc_sw128(ds_tile(qdpos), kTileRows * 128, 1024);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-              const uint64_t off = static_cast<uint64_t>((ks * 2048) >> 4);
+              const uint32_t off = static_cast<uint32_t>((ks * 2048) >> 4);
               umma_ss(tmem + L::kColDQ, ds_mn + off, k_mn + off, id_dq, ks > 0 ? 1u : 0u);
             }
             umma_commit(BAR(L::DQ_FULL));
@@ -1259,13 +1259,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
       constexpr uint32_t id_acc = idesc_bf16_f32(128, D, false, true);
       // Descriptors built once (see the dK/dV kernel): Q and dO K-major for
       // S and dP; the K/V stages K-major for S and dP, K MN-major for dQ and B.
-      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
-      const uint64_t qdesc = sdesc_sw128(sbase + L::kQOff, 16, 1024);
-      const uint64_t dodesc = sdesc_sw128(sbase + L::kDoOff, 16, 1024);
-      const uint64_t kv_k0 = sdesc_sw128(sbase + L::kKvOff, 16, 1024);
-      const uint64_t kv_mn0 = sdesc_sw128(sbase + L::kKvOff, kTileRows * 128, 1024);
-      auto kv_k = [&](uint32_t pos) { return kv_k0 + static_cast<uint64_t>(pos % S) * (2 * kTileUnits); };
-      auto kv_mn = [&](uint32_t pos) { return kv_mn0 + static_cast<uint64_t>(pos % S) * (2 * kTileUnits); };
+      constexpr uint32_t kTileUnits = L::kTileBytes >> 4;
+      const SDesc qdesc = sdesc_sw128(sbase + L::kQOff, 16, 1024);
+      const SDesc dodesc = sdesc_sw128(sbase + L::kDoOff, 16, 1024);
+      const SDesc kv_k0 = sdesc_sw128(sbase + L::kKvOff, 16, 1024);
+      const SDesc kv_mn0 = sdesc_sw128(sbase + L::kKvOff, kTileRows * 128, 1024);
+      auto kv_k = [&](uint32_t pos) { return kv_k0 + (pos % S) * (2 * kTileUnits); };
+      auto kv_mn = [&](uint32_t pos) { return kv_mn0 + (pos % S) * (2 * kTileUnits); };
       uint32_t qn = 0, kvpos = 0, dn = 0;
       SchedIter it = sched_begin(sp);
       int head, i;
@@ -1279,18 +1279,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
         ++qn;
         // S = Q K^T and dP = dO V^T of one key tile: M = 128 queries,
         // N = 128 keys, K = d
-        auto issue_s = [&](uint64_t kd) {
+        auto issue_s = [&](SDesc kd) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
             umma_ss(tmem + L::kColS, qdesc + off, kd + off, id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::S_FULL));
         };
-        auto issue_dp = [&](uint64_t vd) {
+        auto issue_dp = [&](SDesc vd) {
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
             umma_ss(tmem + L::kColDP, dodesc + off, vd + off, id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::DP_FULL));
@@ -1308,14 +1308,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
         // columns [64 w, 64 w + 32), its dS in dP columns [64 w, 64 w + 32).
         for (int jt = 0; jt < nk; ++jt) {
           const uint32_t s = kvpos % S;
-          const uint64_t kmn = kv_mn(kvpos);
+          const SDesc kmn = kv_mn(kvpos);
           ok = wait_bounded(BAR(L::P_READY), dn & 1, wc, SITE_Q_MMA_P, unit);
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {  // B += P K, for the delta correction
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColB, tmem + L::kColS + acol, kmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
+            umma_ts(tmem + L::kColB, tmem + L::kColS + acol, kmn + static_cast<uint32_t>((ks * 2048) >> 4), id_acc,
                     (jt > 0 || ks > 0) ? 1u : 0u);
           }
           const bool more = jt + 1 < nk;
@@ -1332,7 +1332,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t acol = 64 * (ks >> 2) + 8 * (ks & 3);
-            umma_ts(tmem + L::kColDQ, tmem + L::kColDP + acol, kmn + static_cast<uint64_t>((ks * 2048) >> 4), id_acc,
+            umma_ts(tmem + L::kColDQ, tmem + L::kColDP + acol, kmn + static_cast<uint32_t>((ks * 2048) >> 4), id_acc,
                     (jt > 0 || ks > 0) ? 1u : 0u);
           }
           umma_commit(BAR(L::KV_EMPTY + s));

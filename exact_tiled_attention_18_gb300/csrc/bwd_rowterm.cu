@@ -352,10 +352,10 @@ __global__ void __launch_bounds__(kRowThreads, 1)
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
-      const uint64_t qdesc = sdesc_sw128(sbase + L::kQOff, 16, 1024);
-      const uint64_t dodesc = sdesc_sw128(sbase + L::kDoOff, 16, 1024);
-      const uint64_t kv0 = sdesc_sw128(sbase + L::kKvOff, 16, 1024);
+      constexpr uint32_t kTileUnits = L::kTileBytes >> 4;
+      const SDesc qdesc = sdesc_sw128(sbase + L::kQOff, 16, 1024);
+      const SDesc dodesc = sdesc_sw128(sbase + L::kDoOff, 16, 1024);
+      const SDesc kv0 = sdesc_sw128(sbase + L::kKvOff, 16, 1024);
       uint32_t qn = 0, kvpos = 0, tn = 0;
       SchedIter it = sched_begin(sp);
       int head, i;
@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(kRowThreads, 1)
         for (int jt = 0; jt < nk; ++jt, ++tn, ++kvpos) {
           const uint32_t s = kvpos % S;
           const uint32_t b = tn & 1, use = tn >> 1;
-          const uint64_t kd = kv0 + static_cast<uint64_t>(s) * (2 * kTileUnits);
-          const uint64_t vd = kd + kTileUnits;
+          const SDesc kd = kv0 + static_cast<uint32_t>(s) * (2 * kTileUnits);
+          const SDesc vd = kd + kTileUnits;
           ok = wait_bounded(BAR(L::KV_FULL + s), (kvpos / S) & 1, wc, SITE_R_MMA_KV, unit);
           if (!ok) break;
           ok = wait_bounded(BAR(L::S_FREE + b), (use & 1) ^ 1, wc, SITE_R_MMA_SFREE, unit);
@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
           const uint32_t tD = tmem + b * L::kBufCols + L::kColDP;
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
             umma_ss(tS, qdesc + off, kd + off, id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::S_FULL + b));
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kRowThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+            const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
             umma_ss(tD, dodesc + off, vd + off, id_s, ks > 0 ? 1u : 0u);
           }
           umma_commit(BAR(L::DP_FULL + b));

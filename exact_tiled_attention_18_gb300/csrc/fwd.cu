@@ -569,27 +569,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // Descriptors built once: Q tiles for the whole kernel, K (K-major) and
       // V (MN-major) per ring slot.  The K step only moves the start-address
       // field (bits 0-13, 16-byte units), a plain add on the low word.
-      const uint64_t qdesc0 = sdesc_sw128(sbase + L::kQOff, 16, 1024);
-      const uint64_t kdesc0 = sdesc_sw128(sbase + L::kRingOff, 16, 1024);
-      const uint64_t vdesc0 = sdesc_sw128(sbase + L::kRingOff, kTileRows * 128, 1024);
-      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;  // one tile in the address field's 16-byte units
+      const SDesc qdesc0 = sdesc_sw128(sbase + L::kQOff, 16, 1024);
+      const SDesc kdesc0 = sdesc_sw128(sbase + L::kRingOff, 16, 1024);
+      const SDesc vdesc0 = sdesc_sw128(sbase + L::kRingOff, kTileRows * 128, 1024);
+      constexpr uint32_t kTileUnits = L::kTileBytes >> 4;  // one tile in the address field's 16-byte units
       // S_t = Q_t K^T : M=128 query rows, N=128 keys, K=d (both K-major)
       auto issue_s = [&](int t, uint32_t slot) {
-        const uint64_t qd = qdesc0 + static_cast<uint64_t>(t) * kTileUnits;
-        const uint64_t kd = kdesc0 + static_cast<uint64_t>(slot) * kTileUnits;
+        const SDesc qd = qdesc0 + static_cast<uint32_t>(t) * kTileUnits;
+        const SDesc kd = kdesc0 + slot * kTileUnits;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+          const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
           umma_ss(tmem + static_cast<uint32_t>(t * 128), qd + off, kd + off, id_s, ks > 0 ? 1u : 0u);
         }
       };
       // O_t += P_t V : M=128, N=d, K=128 keys; P from TMEM, V MN-major
       auto issue_pv = [&](int t, uint32_t slot, bool acc) {
-        const uint64_t vd = vdesc0 + static_cast<uint64_t>(slot) * kTileUnits;
+        const SDesc vd = vdesc0 + slot * kTileUnits;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           umma_ts(tmem + L::kColO + static_cast<uint32_t>(t * D), tmem + static_cast<uint32_t>(t * 128 + ks * 8),
-                  vd + static_cast<uint64_t>((ks * 2048) >> 4), id_pv, (acc || ks > 0) ? 1u : 0u);
+                  vd + static_cast<uint32_t>((ks * 2048) >> 4), id_pv, (acc || ks > 0) ? 1u : 0u);
         }
       };
       uint32_t qn = 0, kvbase = 0, pn0 = 0, pn1 = 0;

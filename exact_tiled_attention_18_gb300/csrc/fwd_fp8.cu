@@ -339,22 +339,22 @@ __global__ void __launch_bounds__(kF8Threads, 1)
       constexpr uint32_t id_mma = idesc_e4m3_f32(128, 128);  // both products: M = N = 128
       // K-major 128-byte-swizzled tiles; a K step of 32 one-byte elements
       // moves the start-address field by 32 bytes (2 units)
-      const uint64_t qdesc0 = sdesc_sw128(sbase + L::kQOff, 16, 1024);
-      const uint64_t pdesc0 = sdesc_sw128(sbase + L::kPOff, 16, 1024);
-      const uint64_t rdesc0 = sdesc_sw128(sbase + L::kRingOff, 16, 1024);
-      constexpr uint64_t kTileUnits = L::kTileBytes >> 4;
+      const SDesc qdesc0 = sdesc_sw128(sbase + L::kQOff, 16, 1024);
+      const SDesc pdesc0 = sdesc_sw128(sbase + L::kPOff, 16, 1024);
+      const SDesc rdesc0 = sdesc_sw128(sbase + L::kRingOff, 16, 1024);
+      constexpr uint32_t kTileUnits = L::kTileBytes >> 4;
       // S_t = Q_t K^T : M = 128 queries, N = 128 keys, K = d
       auto issue_s = [&](int t, uint32_t slot) {
-        const uint64_t qd = qdesc0 + static_cast<uint64_t>(t) * kTileUnits;
-        const uint64_t kd = rdesc0 + static_cast<uint64_t>(slot) * kTileUnits;
+        const SDesc qd = qdesc0 + static_cast<uint32_t>(t) * kTileUnits;
+        const SDesc kd = rdesc0 + slot * kTileUnits;
 #pragma unroll
         for (int ks = 0; ks < D / 32; ++ks)
           umma_ss_f8(tmem + static_cast<uint32_t>(t * 128), qd + 2 * ks, kd + 2 * ks, id_mma, ks > 0 ? 1u : 0u);
       };
       // O_t += P_t V : M = 128 queries, N = d, K = 128 keys; B is the V^T tile
       auto issue_pv = [&](int t, uint32_t slot, bool acc) {
-        const uint64_t pd = pdesc0 + static_cast<uint64_t>(t) * kTileUnits;
-        const uint64_t vd = rdesc0 + static_cast<uint64_t>(slot) * kTileUnits;
+        const SDesc pd = pdesc0 + static_cast<uint32_t>(t) * kTileUnits;
+        const SDesc vd = rdesc0 + slot * kTileUnits;
 #pragma unroll
         for (int ks = 0; ks < kTileRows / 32; ++ks)
           umma_ss_f8(tmem + L::kColO + static_cast<uint32_t>(t * D), pd + 2 * ks, vd + 2 * ks, id_mma,
