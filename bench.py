@@ -88,7 +88,7 @@ def parse_args(argv=None):
                    help="general additive mask (fa_fwd_bias / fa_bwd_bias) on the training workloads")
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--e2e-chunks", type=int, default=4,
-                   help="batch chunks in flight in the end-to-end pipeline (copies overlap kernels)")
+                   help="chunks of (batch, head) pairs in flight in the end-to-end pipeline (copies overlap kernels)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args(argv)
 
@@ -409,7 +409,7 @@ def run_ours(args):
                                     [o, lse] + ([dq, dk, dv] if do_bwd else []))}
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-        chunks = max(c for c in range(1, min(args.e2e_chunks, B) + 1) if B % c == 0)
+        chunks = max(c for c in range(1, min(args.e2e_chunks, B * H) + 1) if (B * H) % c == 0)
         pipe = HostStepPipeline(B, H, N, d, w.causal, w.scale, chunks=chunks, device=device, backward=do_bwd)
         pipe.step(host_in, host_out)
         pipe.synchronize()

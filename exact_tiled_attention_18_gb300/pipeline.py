@@ -1,7 +1,9 @@
 """Training step on a batch held in pinned host memory, with the copies hidden.
 
-Heads are independent, so a batch can be cut along B into chunks whose
-host->device copies, kernels and device->host copies run on three streams:
+Heads are independent, so a batch can be cut into chunks of consecutive
+(batch, head) pairs (rows of the [B*H, N, d] view, contiguous in host and
+device memory) whose host->device copies, kernels and device->host copies run
+on three streams:
 while chunk k computes, chunk k+1's inputs come in and chunk k-1's results go
 out (the copy engines and the SMs work at the same time).  Every computation
 is the C ABI's forward and backward (fa_fwd, fa_bwd) on each chunk; this
@@ -18,35 +20,36 @@ class HostStepPipeline:
     live in pinned host memory and whose results (O, LSE, dQ, dK, dV) go back
     to pinned host memory.
 
-    ``chunks`` pieces along B are in flight at once; device buffers for each
-    piece are allocated once here and reused by every ``step``.
+    ``chunks`` pieces of B*H/chunks (batch, head) pairs each are in flight at
+    once; device buffers for each piece are allocated once here and reused by
+    every ``step``.
     """
 
     def __init__(self, B: int, H: int, N: int, d: int, causal: bool, scale: float, chunks: int = 2,
                  device=None, backward: bool = True):
         import torch
-        if chunks < 1 or B % chunks != 0:
-            raise ValueError("chunks must divide B")
+        if chunks < 1 or (B * H) % chunks != 0:
+            raise ValueError("chunks must divide B*H")
         self.B, self.H, self.N, self.d = B, H, N, d
         self.causal, self.scale, self.backward = causal, scale, backward
         self.chunks = chunks
-        self.cb = B // chunks
+        self.ch = B * H // chunks  # (batch, head) pairs per chunk
         self.device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         self.s_in = torch.cuda.Stream(self.device)
         self.s_cmp = torch.cuda.Stream(self.device)
         self.s_out = torch.cuda.Stream(self.device)
-        shp = (self.cb, H, N, d)
+        shp = (1, self.ch, N, d)  # one "batch" of ch heads
         bf, f32 = torch.bfloat16, torch.float32
         self.bufs = []
         for _ in range(chunks):
             b = {n: torch.empty(shp, dtype=bf, device=self.device) for n in ("q", "k", "v")}
             b["o"] = torch.empty(shp, dtype=f32, device=self.device)
-            b["lse"] = torch.empty((self.cb, H, N), dtype=f32, device=self.device)
+            b["lse"] = torch.empty((1, self.ch, N), dtype=f32, device=self.device)
             if backward:
                 b["do"] = torch.empty(shp, dtype=bf, device=self.device)
                 for n in ("dq", "dk", "dv"):
                     b[n] = torch.empty(shp, dtype=f32, device=self.device)
-                b["ws"] = torch.empty(binding.fa_bwd_workspace_bytes(self.cb, H, N) // 4, dtype=f32,
+                b["ws"] = torch.empty(binding.fa_bwd_workspace_bytes(1, self.ch, N) // 4, dtype=f32,
                                       device=self.device)
             self.bufs.append(b)
         # per chunk: inputs consumed by the kernels / results copied out
@@ -60,14 +63,19 @@ class HostStepPipeline:
         import torch
         ins = ("q", "k", "v") + (("do",) if self.backward else ())
         outs = ("o", "lse") + (("dq", "dk", "dv") if self.backward else ())
+        BH = self.B * self.H
+
+        def rows(t):  # the [B*H, ...] view of a [B, H, ...] host tensor
+            return t.view((BH,) + tuple(t.shape[2:]))
+
         for c in range(self.chunks):
-            sl = slice(c * self.cb, (c + 1) * self.cb)
+            sl = slice(c * self.ch, (c + 1) * self.ch)
             b = self.bufs[c]
             with torch.cuda.stream(self.s_in):
                 if self.in_free[c] is not None:
                     self.s_in.wait_event(self.in_free[c])
                 for n in ins:
-                    b[n].copy_(host_in[n][sl], non_blocking=True)
+                    b[n][0].copy_(rows(host_in[n])[sl], non_blocking=True)
                 arrived = torch.cuda.Event()
                 arrived.record(self.s_in)
             with torch.cuda.stream(self.s_cmp):
@@ -85,7 +93,7 @@ class HostStepPipeline:
             with torch.cuda.stream(self.s_out):
                 self.s_out.wait_event(done)
                 for n in outs:
-                    host_out[n][sl].copy_(b[n], non_blocking=True)
+                    rows(host_out[n])[sl].copy_(b[n][0], non_blocking=True)
                 copied = torch.cuda.Event()
                 copied.record(self.s_out)
                 self.out_free[c] = copied

@@ -1,5 +1,6 @@
-"""HostStepPipeline: a training step on pinned host tensors, chunked along B so
-that copies overlap kernels, gives exactly the results of direct calls."""
+"""HostStepPipeline: a training step on pinned host tensors, cut into chunks of
+(batch, head) pairs so that copies overlap kernels, gives exactly the results
+of direct calls."""
 
 import pytest
 import torch
@@ -11,7 +12,7 @@ from tests.helpers import scale_for
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("chunks", [1, 2, 4])
+@pytest.mark.parametrize("chunks", [1, 2, 4, 8])
 def test_pipeline_matches_direct_calls(chunks):
     B, H, N, d = 4, 2, 500, 128
     inp = workloads.make_inputs(B, H, N, d, seed=12, with_grad=True)
@@ -35,3 +36,5 @@ def test_pipeline_matches_direct_calls(chunks):
 def test_pipeline_rejects_uneven_chunks():
     with pytest.raises(ValueError):
         fa.HostStepPipeline(3, 1, 128, 64, False, 0.125, chunks=2)
+    with pytest.raises(ValueError):
+        fa.HostStepPipeline(2, 3, 128, 64, False, 0.125, chunks=4)
