@@ -58,8 +58,9 @@ class HostStepPipeline:
 
     def step(self, host_in: dict, host_out: dict):
         """Queue one step: host_in holds pinned q, k, v (and do), host_out
-        pinned o, lse (and dq, dk, dv), all [B, ...].  Returns at once; the
-        results are in host_out after ``synchronize()``."""
+        pinned o, lse (and dq, dk, dv), all [B, H, ...] and contiguous (a
+        chunk is a row range of their [B*H, ...] view; anything else raises).
+        Returns at once; the results are in host_out after ``synchronize()``."""
         import torch
         ins = ("q", "k", "v") + (("do",) if self.backward else ())
         outs = ("o", "lse") + (("dq", "dk", "dv") if self.backward else ())
